@@ -1,0 +1,334 @@
+"""Benchmark of one paged decode step on GB300: copy-on-write copies (if any), the
+append of one new token per sequence, and decode attention through block tables.
+
+Prints ONE JSON line (rank 0).  `value` is the KV bytes decode attends per step
+divided by the device time of a step (GB/s), inputs resident in HBM.  The dominant
+kernel (decode, split-K partitions + merge) is also reported against the HBM
+roofline; `e2e` repeats the step with each step's inputs copied from pinned host
+memory and the output copied back inside the timed region; `cpu_baseline` times
+the float64 oracle on the host's cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention: KV GB/s, seq-tokens/s, fraction of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def elem(dtype):
+    return torch.empty((), dtype=dtype).element_size()
+
+
+def roofline_bytes(w, out_elem):
+    """Algorithmic bytes of one decode: K+V once, q, out, block-table entries, lengths."""
+    e = elem(w.dtype)
+    lens = w.context_lens.to(torch.int64)
+    kv = int(lens.sum()) * 2 * w.num_kv_heads * w.head_dim * e
+    S = w.num_seqs
+    qo = S * w.num_q_heads * w.head_dim * (e + out_elem)
+    table = 4 * int(((lens + w.block_size - 1) // w.block_size).sum()) + 4 * S
+    return kv, kv + qo + table
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    def __init__(self, index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[x.strip() for x in ln.split(",")] for ln in out.splitlines() if ln.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [x for x in sm if mx and x >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, budget_s):
+    """The float64 oracle on this host's cores over the same step, repeated within a budget."""
+    import oracle
+
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    wc = w.to("cpu")
+    oracle.block_copy(wc.cow_pairs, kc, vc)
+    oracle.kv_append(wc.k_new, wc.v_new, wc.slot_mapping, kc, vc)
+    kv_bytes, _ = roofline_bytes(wc, elem(w.dtype))
+    # bounded sample: sequences in order until the first call takes ~budget/3
+    S = wc.num_seqs
+    n = S
+    t0 = time.perf_counter()
+    oracle.attention_decode(wc.q[:1], kc, vc, wc.block_tables[:1], wc.context_lens[:1], wc.scale)
+    one = max(time.perf_counter() - t0, 1e-4)
+    n = max(1, min(S, int((budget_s / 3) / one)))
+    sel = slice(0, n)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < 3 or (time.perf_counter() < t_end and len(times) < 50):
+        t0 = time.perf_counter()
+        oracle.attention_decode(wc.q[sel], kc, vc, wc.block_tables[sel], wc.context_lens[sel], wc.scale)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end and len(times) >= 3:
+            break
+    sample_lens = wc.context_lens[sel].to(torch.int64)
+    sample_kv = int(sample_lens.sum()) * 2 * w.num_kv_heads * w.head_dim * elem(w.dtype)
+    t = statistics.median(times)
+    return {"value": sample_kv / t / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {S} sequences ({int(sample_lens.sum())} tokens), median of {len(times)} calls",
+            "seq_tokens_per_s": int(sample_lens.sum()) / t, "seconds_per_call": t, "_kv_bytes": kv_bytes}
+
+
+def run_reference(args):
+    """--impl reference: the float64 oracle timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workloads.make_workload(args.config, canary=False)
+    import oracle
+
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    oracle.block_copy(w.cow_pairs, kc, vc)
+    oracle.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    t0 = time.perf_counter()
+    oracle.attention_decode(w.q[:1], kc, vc, w.block_tables[:1], w.context_lens[:1], w.scale)
+    one = max(time.perf_counter() - t0, 1e-4)
+    # each step: a bounded sample of sequences, sized so the whole run takes ~1-2 minutes
+    per_step = 60.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(w.num_seqs, int(per_step / one)))
+    sel = slice(0, n)
+
+    def step():
+        oracle.attention_decode(w.q[sel], kc, vc, w.block_tables[sel], w.context_lens[sel], w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    lens = w.context_lens[sel].to(torch.int64)
+    kv = int(lens.sum()) * 2 * w.num_kv_heads * w.head_dim * elem(w.dtype)
+    value = kv / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_sequences": n, "num_seqs": w.num_seqs},
+            "seq_tokens_per_s": int(lens.sum()) / dt,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{n} of {w.num_seqs} sequences per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import paged_kv_cache_310_gb300 as pkv
+
+    path = {"auto": pkv.PATH_AUTO, "cuda_core": pkv.PATH_CUDA_CORE, "tensor_core": pkv.PATH_TENSOR_CORE}[args.path]
+    # every rank decodes its own batch of the same workload shape (independent replicas)
+    w = workloads.make_workload(args.config, canary=False, pool_device=dev)
+    g = w.to(dev)
+    S, Hq, D = g.q.shape
+    out = torch.empty((S, Hq, D), dtype=w.dtype, device=dev)
+    maxL = w.max_context_len
+    host_pairs = w.cow_pairs.cpu()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q, kn, vn, slots, tables, lens):
+        if g.cow_pairs.numel():
+            pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache)
+        pkv.paged_kv_append(kn, vn, slots, g.k_cache, g.v_cache)
+        e_mid = torch.cuda.Event(enable_timing=True)
+        e_mid.record(stream)
+        pkv.paged_attention_decode(q, g.k_cache, g.v_cache, tables, lens, w.scale, out, max_context_len=maxL,
+                                   path=path, partition_tokens=args.partition)
+        return e_mid
+
+    args_dev = (g.q, g.k_new, g.v_new, g.slot_mapping, g.block_tables, g.context_lens)
+    if g.cow_pairs.numel():  # validate the pairs once on the host
+        pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache, host_pairs=host_pairs)
+    for _ in range(max(3, args.warmup)):
+        step(*args_dev)
+    torch.cuda.synchronize()
+    if pkv.device_error() != 0:
+        raise SystemExit("device error flag set during warm-up")
+
+    launches_per_step = (1 if g.cow_pairs.numel() else 0) + 1 + 1
+    ws_parts = pkv.paged_attention_workspace_bytes(S, Hq, maxL, g.k_cache, path=path,
+                                                   partition_tokens=args.partition) > 0
+    launches_per_step += 1 if ws_parts else 0
+
+    # ---------------- device-timed region ----------------
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = []
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        mids.append(step(*args_dev))
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    decode_ms = statistics.mean(m.elapsed_time(e) for m, e in zip(mids, ends))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t)
+    if pkv.device_error() != 0:
+        raise SystemExit("device error flag set in the timed region")
+    ms_per_step = total_ms / args.steps
+
+    # ---------------- end to end: host inputs in, host output out ----------------
+    pinned_in = [t.cpu().pin_memory() for t in (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
+                                                 w.context_lens)]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = [torch.empty_like(t, device=dev) for t in pinned_in]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+    d2h = out_host.numel() * out_host.element_size()
+    n_e2e = max(3, args.e2e_steps)
+    for i in range(3 + n_e2e):
+        if i == 3:
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for d, h in zip(dev_in, pinned_in):
+            d.copy_(h, non_blocking=True)
+        step(*dev_in)
+        out_host.copy_(out, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t)
+
+    kv_bytes, algo_bytes = roofline_bytes(w, elem(out.dtype))
+    peak, peak_kind = peaks()
+    tokens = int(w.context_lens.sum())
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": workloads.DTYPE_NAMES[w.dtype], "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": D, "block_size": w.block_size, "sum_context_tokens": tokens,
+                   "kv_bytes_per_step": kv_bytes, "path": args.path, "partition_tokens": args.partition,
+                   "l2": f"inputs larger than L2 (KV {kv_bytes / 1e9:.2f} GB > 129 MB): no flush",
+                   "parallelism": f"replicas x{world}"},
+        "seq_tokens_per_s": world * tokens / (ms_per_step * 1e-3),
+        "hbm_frac_step": (algo_bytes / (ms_per_step * 1e-3) / 1e9) / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "kernel": "paged_attention_decode (partition kernel + merge)",
+                     "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": decode_ms},
+        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w, args.cpu_seconds)
+        cb.pop("_kv_bytes", None)
+        result["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

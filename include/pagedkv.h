@@ -1,0 +1,185 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the data-parallel hot path of PagedAttention
+ * on one GB300 (sm_103a).
+ *
+ * The method (four web pages on PagedAttention / vLLM):
+ *  - "anthology-of-the-sota note-023", Method: a sequence's KV cache is cut into
+ *    fixed-size blocks of a fixed number of tokens; a per-sequence block table maps
+ *    logical block i to a physical block; attention gathers K/V from those
+ *    non-contiguous blocks; blocks are allocated as the sequence grows and shared
+ *    between sequences, with copy-on-write when one of them diverges.
+ *  - "Efficient Memory Management for Large Language Model Serving with
+ *    PagedAttention", How It Works: blocks of e.g. 16 tokens; the block table plays
+ *    the part of an OS page table; copy-on-write for parallel sampling / beam search.
+ *  - "Paged Attention" glossary, paragraph 4: attention's arithmetic is unchanged,
+ *    only the storage of K/V moves; GQA paragraph: several query heads share one
+ *    key/value head (Llama 2 70B: 64 query heads, 8 KV heads).
+ *
+ * Layouts (the pages fix none; this library's reading):
+ *  - k_cache, v_cache: [num_blocks][num_kv_heads][block_size][head_dim], row-major.
+ *    One (block, kv head) tile is block_size*head_dim contiguous elements.
+ *  - q, out: [num_seqs][num_q_heads][head_dim].  Query head h reads KV head
+ *    h / (num_q_heads / num_kv_heads).
+ *  - k, v of new tokens: [num_tokens][num_kv_heads][head_dim].
+ *  - block_tables: int32 [num_seqs][max_blocks_per_seq]; entry i of row s is the
+ *    physical block of logical block i of sequence s.  Entries at or past
+ *    ceil(context_lens[s] / block_size) are never read.
+ *  - context_lens: int32 [num_seqs], tokens each sequence attends over (>= 0).
+ *  - slot_mapping: int64 [num_tokens]; slot = physical_block * block_size + row;
+ *    a negative slot is padding and is skipped.
+ *  - src_dst_pairs: int64 [num_pairs][2] of (source block, destination block).
+ *
+ * Conventions:
+ *  - Ownership: the caller owns every buffer.  Apart from arguments documented as
+ *    host memory, every pointer is device memory of the current device.  The
+ *    library allocates no device memory, keeps no pointer after a call returns,
+ *    and needs caller-provided workspace only for split-K decode.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call only enqueues work and returns; results are ready when the stream is.
+ *  - Alignment: q, k, v, out, k_cache, v_cache must be 16-byte aligned, and
+ *    head_dim * element size must be a multiple of 16 bytes.
+ *  - Errors: a call returns PKV_OK or an error status and records a message that
+ *    paged_kv_last_error() returns (per host thread).  Host checks cover shapes,
+ *    scalars, pointers and alignment.  Device-side index faults never trap: a
+ *    kernel that meets an out-of-range block id or slot, or a bounded wait that
+ *    runs out, sets a device flag, skips the access and completes;
+ *    paged_kv_device_error() reports and clears that flag.
+ *  - Supported set: dtype f32, f16, bf16 (q, k, v, caches share it); out dtype
+ *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16 or 32;
+ *    num_q_heads a multiple of num_kv_heads with group size <= 8.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,    /* bad pointer, shape, scalar or alignment */
+  PKV_ERR_UNSUPPORTED = 2,    /* outside the supported set above */
+  PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+  PKV_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  PKV_ERR_DEVICE_INDEX = 5,   /* a kernel met an out-of-range block id, slot or length */
+  PKV_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out (copy never landed) */
+} pkv_status;
+
+/* Geometry of one layer's block pool (both k_cache and v_cache). */
+typedef struct {
+  int32_t num_blocks;   /* physical blocks in the pool */
+  int32_t block_size;   /* tokens per block: 8, 16 or 32 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* 64 or 128 */
+  int32_t dtype;        /* pkv_dtype of the caches, q, k and v */
+} pkv_cache_desc;
+
+/* Decode path selection and split-K partition size (NULL config = automatic). */
+typedef enum { PKV_PATH_AUTO = 0, PKV_PATH_CUDA_CORE = 1, PKV_PATH_TENSOR_CORE = 2 } pkv_path;
+
+typedef struct {
+  int32_t path;              /* pkv_path */
+  int32_t partition_tokens;  /* 0 = automatic, else a positive multiple of 128 */
+} pkv_decode_config;
+
+/*
+ * paged_kv_append -- write new tokens' K and V into their cache slots.
+ * Pages: "Efficient Memory Management ... with PagedAttention", How It Works (blocks
+ * filled as tokens are generated, allocated on demand); note-023, Method.
+ *
+ * For each token t with slot_mapping[t] >= 0 and every KV head h:
+ *   k_cache[slot / block_size][h][slot % block_size][:] = k[t][h][:], same for v.
+ * Bit-exact copies.  Slots must be distinct (duplicates race).  A slot
+ * >= num_blocks * block_size sets the device index flag and is skipped.
+ * k, v: device [num_tokens][num_kv_heads][head_dim]; slot_mapping: device int64.
+ */
+pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, void* k_cache, void* v_cache,
+                           const pkv_cache_desc* cache, void* stream);
+
+/*
+ * paged_block_copy -- copy-on-write divergence: block dst becomes a copy of block
+ * src in both pools (all KV heads and rows).
+ * Pages: note-023, Concepts (copy-on-write gives the writer its own copy of a shared
+ * block); "Paged Attention" glossary, paragraph 2; "Efficient Memory Management ...",
+ * How It Works (copy when a sequence sharing a prefix diverges).
+ *
+ * src_dst_pairs: device int64 [num_pairs][2].  host_pairs: optional host copy of the
+ * same pairs; when given, the call checks every id is in [0, num_blocks), src != dst,
+ * no dst repeats and no dst is also a src (PKV_ERR_INVALID_ARG otherwise).  Without
+ * it, out-of-range ids set the device index flag and are skipped; overlapping pairs
+ * are the caller's responsibility.  Bit-exact.
+ */
+pkv_status paged_block_copy(const int64_t* src_dst_pairs, const int64_t* host_pairs,
+                            int32_t num_pairs, void* k_cache, void* v_cache,
+                            const pkv_cache_desc* cache, void* stream);
+
+/*
+ * Bytes of workspace paged_attention_decode needs for these sizes and config
+ * (0 when every sequence fits one partition).  max_context_len: host upper bound on
+ * context_lens.  Returns 0 for invalid arguments as well (then the decode call
+ * itself reports the error).
+ */
+size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t max_context_len, const pkv_cache_desc* cache,
+                                       const pkv_decode_config* config);
+
+/*
+ * paged_attention_decode -- single-token decode attention through block tables.
+ * Pages: note-023, Method and Concepts (attention gathers K/V through the block
+ * table from non-contiguous blocks); "Paged Attention" glossary, paragraph 4
+ * (arithmetic unchanged) and GQA paragraph.
+ *
+ * For every sequence s and query head h, with n = context_lens[s], kv = h / G,
+ * K_j / V_j = row j % block_size of physical block block_tables[s][j / block_size]:
+ *   out[s][h][:] = sum_j softmax_j(scale * q[s][h] . K_j) V_j,   j < n;
+ *   n == 0 gives zeros.  Accumulation in fp32; out rounded to out_dtype (RNE).
+ * Sequences longer than the partition size are split into partitions whose
+ * (max, sum, unnormalised output) go to the workspace and are merged by a second
+ * kernel.  max_context_len: host upper bound on context_lens (a longer sequence
+ * sets the device index flag).  workspace: device, at least
+ * paged_attention_workspace_bytes(...) bytes, 256-byte aligned; NULL allowed when
+ * that is 0.  out must not alias any input.
+ */
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len, float scale,
+                                  void* out, int32_t out_dtype, void* workspace,
+                                  size_t workspace_bytes, const pkv_cache_desc* cache,
+                                  const pkv_decode_config* config, void* stream);
+
+/*
+ * paged_kv_gather -- the block-table lookup alone (testing the indexing bit-exactly):
+ * k_out[s][h][j][:] = k_cache[block_tables[s][j / bs]][h][j % bs][:] for j < n_s,
+ * same for v.  Rows j >= context_lens[s] are not written.
+ * k_out, v_out: device [num_seqs][num_kv_heads][max_context_len][head_dim].
+ */
+pkv_status paged_kv_gather(const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t max_context_len, void* k_out, void* v_out,
+                           const pkv_cache_desc* cache, void* stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* paged_kv_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error flag of the current
+ * device: PKV_OK, PKV_ERR_DEVICE_INDEX or PKV_ERR_DEVICE_TIMEOUT (PKV_ERR_CUDA if
+ * the synchronisation itself fails).
+ */
+pkv_status paged_kv_device_error(void* stream);
+
+/* Library version, e.g. "0.1.0". */
+const char* paged_kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

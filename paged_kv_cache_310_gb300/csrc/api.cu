@@ -1,0 +1,299 @@
+// api.cu -- the extern "C" entry points of libpagedkv.so (declared in
+// include/pagedkv.h): argument checks, launch configuration, the device error flag.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+// One error flag per device that loads the library.  Kernels OR bits into it
+// instead of trapping; paged_kv_device_error() reads and clears it.
+__device__ int g_device_error;
+
+thread_local std::string t_last_error;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_flag_mutex;
+int* g_flag_ptr[kMaxDevices] = {};
+
+// Device address of g_device_error on the current device (looked up once per device).
+pkv_status device_flag(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lock(g_flag_mutex);
+  if (!g_flag_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error flag)");
+    g_flag_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_flag_ptr[dev];
+  return PKV_OK;
+}
+
+size_t elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+  if (c->dtype < PKV_F32 || c->dtype > PKV_BF16)
+    return fail(PKV_ERR_UNSUPPORTED, "cache dtype %d", c->dtype);
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks %d, num_kv_heads %d must be positive",
+                c->num_blocks, c->num_kv_heads);
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", c->block_size);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+  if (c->num_kv_heads > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d", c->num_kv_heads);
+  return PKV_OK;
+}
+
+struct DecodePlan {
+  int path;         // PKV_PATH_CUDA_CORE (the tensor-core path is added separately)
+  int part_tokens;  // tokens per partition, multiple of 128
+  int max_parts;    // partitions of the longest sequence
+  size_t workspace; // bytes
+};
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
+                       const pkv_cache_desc* c, const pkv_decode_config* cfg, DecodePlan* plan) {
+  if (pkv_status st = check_cache(c)) return st;
+  if (num_seqs < 0 || num_seqs > 65535)
+    return fail(PKV_ERR_INVALID_ARG, "num_seqs %d outside [0, 65535]", num_seqs);
+  if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, c->num_kv_heads);
+  const int group = num_q_heads / c->num_kv_heads;
+  if (group > 8) return fail(PKV_ERR_UNSUPPORTED, "query-head group %d > 8", group);
+  if (max_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d < 0", max_len);
+  const int path = cfg ? cfg->path : PKV_PATH_AUTO;
+  if (path != PKV_PATH_AUTO && path != PKV_PATH_CUDA_CORE)
+    return fail(PKV_ERR_UNSUPPORTED, "decode path %d not available", path);
+  int part = cfg ? cfg->partition_tokens : 0;
+  if (part < 0 || part % 128 || part > 16384)
+    return fail(PKV_ERR_INVALID_ARG, "partition_tokens %d: need 0 or a multiple of 128 <= 16384", part);
+  if (part == 0) part = max_len <= 512 ? (max_len < 128 ? 128 : round_up(max_len, 128)) : 512;
+  plan->path = PKV_PATH_CUDA_CORE;
+  plan->part_tokens = part;
+  plan->max_parts = max_len == 0 ? 1 : (max_len + part - 1) / part;
+  plan->workspace = 0;
+  if (plan->max_parts > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan->max_parts;
+    const size_t ml = (rows * 2 * sizeof(float) + 255) / 256 * 256;
+    plan->workspace = ml + rows * c->head_dim * sizeof(float);
+  }
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* paged_kv_version(void) { return "0.1.0"; }
+
+const char* paged_kv_last_error(void) { return t_last_error.c_str(); }
+
+pkv_status paged_kv_device_error(void* stream) {
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int value = 0;
+  e = cudaMemcpy(&value, flag, sizeof value, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error flag");
+  if (value) {
+    const int zero = 0;
+    e = cudaMemcpy(flag, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error flag");
+  }
+  if (value & kErrTimeout) return fail(PKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (flag 0x%x)", value);
+  if (value) return fail(PKV_ERR_DEVICE_INDEX, "a kernel met an out-of-range index or length (flag 0x%x)", value);
+  return PKV_OK;
+}
+
+pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, void* k_cache, void* v_cache,
+                           const pkv_cache_desc* cache, void* stream) {
+  if (pkv_status st = check_cache(cache)) return st;
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID_ARG, "k, v and the caches must be 16-byte aligned");
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  const int row_bytes = static_cast<int>(cache->head_dim * elem_bytes(cache->dtype));
+  cudaError_t e = launch_append(k, v, slot_mapping, num_tokens, k_cache, v_cache,
+                                cache->num_kv_heads, cache->block_size, row_bytes,
+                                static_cast<int64_t>(cache->num_blocks) * cache->block_size, flag,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "append launch");
+}
+
+pkv_status paged_block_copy(const int64_t* src_dst_pairs, const int64_t* host_pairs,
+                            int32_t num_pairs, void* k_cache, void* v_cache,
+                            const pkv_cache_desc* cache, void* stream) {
+  if (pkv_status st = check_cache(cache)) return st;
+  if (num_pairs < 0 || num_pairs > 65535)
+    return fail(PKV_ERR_INVALID_ARG, "num_pairs %d outside [0, 65535]", num_pairs);
+  if (num_pairs == 0) return PKV_OK;
+  if (!src_dst_pairs || !k_cache || !v_cache) return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PKV_ERR_INVALID_ARG, "the caches must be 16-byte aligned");
+  if (host_pairs) {
+    // copy-on-write pairs: ids in range, src != dst, no dst twice, no dst also a src
+    std::string seen_dst(static_cast<size_t>(cache->num_blocks), 0), seen_src(seen_dst);
+    for (int32_t i = 0; i < num_pairs; ++i) {
+      const int64_t a = host_pairs[2 * i], b = host_pairs[2 * i + 1];
+      if (a < 0 || a >= cache->num_blocks || b < 0 || b >= cache->num_blocks)
+        return fail(PKV_ERR_INVALID_ARG, "pair %d (%lld, %lld) outside [0, %d)", i, (long long)a,
+                    (long long)b, cache->num_blocks);
+      if (a == b) return fail(PKV_ERR_INVALID_ARG, "pair %d copies block %lld onto itself", i, (long long)a);
+      if (seen_dst[b]) return fail(PKV_ERR_INVALID_ARG, "destination block %lld appears twice", (long long)b);
+      seen_dst[b] = 1;
+      seen_src[a] = 1;
+    }
+    for (int32_t i = 0; i < num_pairs; ++i)
+      if (seen_src[host_pairs[2 * i + 1]])
+        return fail(PKV_ERR_INVALID_ARG, "block %lld is both a source and a destination",
+                    (long long)host_pairs[2 * i + 1]);
+  }
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  const int64_t block_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size *
+                              cache->head_dim * elem_bytes(cache->dtype);
+  cudaError_t e = launch_block_copy(src_dst_pairs, num_pairs, k_cache, v_cache, block_bytes,
+                                    cache->num_blocks, flag, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "block copy launch");
+}
+
+size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t max_context_len, const pkv_cache_desc* cache,
+                                       const pkv_decode_config* config) {
+  DecodePlan plan;
+  if (plan_decode(num_seqs, num_q_heads, max_context_len, cache, config, &plan) != PKV_OK) return 0;
+  return plan.workspace;
+}
+
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len, float scale,
+                                  void* out, int32_t out_dtype, void* workspace,
+                                  size_t workspace_bytes, const pkv_cache_desc* cache,
+                                  const pkv_decode_config* config, void* stream) {
+  DecodePlan plan;
+  if (pkv_status st = plan_decode(num_seqs, num_q_heads, max_context_len, cache, config, &plan))
+    return st;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !context_lens || !out)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (max_context_len > 0 && !block_tables) return fail(PKV_ERR_INVALID_ARG, "block_tables is NULL");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+  if (out_dtype != cache->dtype && out_dtype != PKV_F32)
+    return fail(PKV_ERR_UNSUPPORTED, "out dtype %d (must be the cache dtype or f32)", out_dtype);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  const int64_t need_blocks = (static_cast<int64_t>(max_context_len) + cache->block_size - 1) / cache->block_size;
+  if (max_blocks_per_seq < need_blocks)
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d < ceil(max_context_len / block_size) = %lld",
+                max_blocks_per_seq, (long long)need_blocks);
+  if (plan.workspace > 0) {
+    if (!workspace || workspace_bytes < plan.workspace)
+      return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.workspace,
+                  workspace ? workspace_bytes : 0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+
+  DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  if (plan.workspace > 0) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.max_parts;
+    const size_t ml = (rows * 2 * sizeof(float) + 255) / 256 * 256;
+    p.ws_ml = static_cast<float*>(workspace);
+    p.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml);
+  }
+  p.err = flag;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = num_q_heads / cache->num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.block_size = cache->block_size;
+  p.num_blocks = cache->num_blocks;
+  p.head_dim = cache->head_dim;
+  p.part_tokens = plan.part_tokens;
+  p.max_parts = plan.max_parts;
+  p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_simt(p, cache->dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = launch_merge(p, cache->dtype, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return PKV_OK;
+}
+
+pkv_status paged_kv_gather(const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens,
+                           int32_t num_seqs, int32_t max_context_len, void* k_out, void* v_out,
+                           const pkv_cache_desc* cache, void* stream) {
+  if (pkv_status st = check_cache(cache)) return st;
+  if (num_seqs < 0 || num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", num_seqs);
+  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d", max_context_len);
+  if (num_seqs == 0 || max_context_len == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_tables || !context_lens || !k_out || !v_out)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out))
+    return fail(PKV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  const int row_bytes = static_cast<int>(cache->head_dim * elem_bytes(cache->dtype));
+  cudaError_t e = launch_gather(k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                num_seqs, max_context_len, k_out, v_out, cache->num_kv_heads,
+                                cache->block_size, row_bytes, cache->num_blocks, flag,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "gather launch");
+}
+
+}  // extern "C"

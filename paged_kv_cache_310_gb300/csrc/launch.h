@@ -1,0 +1,48 @@
+// launch.h -- host-side launchers shared between the translation units of
+// libpagedkv (not part of the public ABI; see include/pagedkv.h for that).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Everything decode kernels need, by value (one __grid_constant__ struct).
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  float* ws_o;   // [S][Hq][max_parts][D] un-normalised partition outputs (fp32)
+  float* ws_ml;  // [S][Hq][max_parts][2] partition (max, sum) in the log2 domain
+  int* err;      // device error flag
+  int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
+  int32_t block_size, num_blocks, head_dim;
+  int32_t part_tokens, max_parts;
+  int32_t out_f32;   // 1: out is fp32, 0: out has the cache dtype
+  float scale_log2;  // softmax scale * log2(e): scores live in the exp2 domain
+};
+
+// CUDA-core split-K decode (any supported dtype, head_dim 64/128, group <= 8).
+cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t stream);
+// Partition merge for sequences longer than one partition.
+cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
+
+cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t num_tokens,
+                          void* k_cache, void* v_cache, int32_t num_kv_heads, int32_t block_size,
+                          int32_t row_bytes, int64_t num_slots, int* err, cudaStream_t stream);
+
+cudaError_t launch_block_copy(const int64_t* pairs, int32_t num_pairs, void* k_cache,
+                              void* v_cache, int64_t block_bytes, int32_t num_blocks, int* err,
+                              cudaStream_t stream);
+
+cudaError_t launch_gather(const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* context_lens,
+                          int32_t num_seqs, int32_t max_len, void* k_out, void* v_out,
+                          int32_t num_kv_heads, int32_t block_size, int32_t row_bytes,
+                          int32_t num_blocks, int* err, cudaStream_t stream);
+
+}  // namespace pkv

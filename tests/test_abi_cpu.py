@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library builds, loads, exports what the header
+declares, and its host-side argument checks answer before any device work."""
+import ctypes
+import subprocess
+
+import pytest
+
+import paged_kv_cache_310_gb300 as pkv
+from paged_kv_cache_310_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.library()
+
+
+def test_header_declares_the_three_calls():
+    names = pkv.declared_functions()
+    for n in ("paged_kv_append", "paged_attention_decode", "paged_block_copy"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.library_path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in pkv.declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version(lib):
+    assert lib.paged_kv_version().decode().count(".") == 2
+
+
+def _desc(num_blocks=64, block_size=16, num_kv_heads=8, head_dim=128, dtype=pkv.BF16):
+    return pkv.CacheDesc(num_blocks, block_size, num_kv_heads, head_dim, dtype)
+
+
+def _ws(lib, S, Hq, L, desc, part=0, path=0):
+    cfg = pkv.DecodeConfig(path, part)
+    return lib.paged_attention_workspace_bytes(S, Hq, L, ctypes.byref(desc), ctypes.byref(cfg))
+
+
+def test_workspace_sizes(lib):
+    d = _desc()
+    assert _ws(lib, 64, 32, 512, d) == 0            # one partition: no workspace
+    n = _ws(lib, 64, 32, 2048, d)                   # 4 partitions of 512
+    rows = 64 * 32 * 4
+    assert n == -(-rows * 8 // 256) * 256 + rows * 128 * 4
+    assert _ws(lib, 64, 32, 2048, d, part=1024) < n
+    assert _ws(lib, 64, 32, 2048, d, part=100) == 0  # invalid partition size
+    assert _ws(lib, 64, 30, 2048, d) == 0            # heads not a multiple of kv heads
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("block_size", 7, 2), ("head_dim", 96, 2), ("dtype", 5, 2), ("num_blocks", 0, 1), ("num_kv_heads", 0, 1),
+])
+def test_cache_descriptor_checks(lib, field, value, status):
+    d = _desc()
+    setattr(d, field, value)
+    rc = lib.paged_kv_append(None, None, None, 1, None, None, ctypes.byref(d), None)
+    assert rc == status
+    assert lib.paged_kv_last_error()
+
+
+def test_argument_checks_before_device_work(lib):
+    d = _desc()
+    assert lib.paged_kv_append(None, None, None, -1, None, None, ctypes.byref(d), None) == 1
+    assert lib.paged_kv_append(None, None, None, 0, None, None, ctypes.byref(d), None) == 0
+    assert lib.paged_kv_append(None, None, None, 3, None, None, ctypes.byref(d), None) == 1
+    assert b"NULL" in lib.paged_kv_last_error()
+    odd = ctypes.c_void_p(0x1008)
+    assert lib.paged_kv_append(odd, odd, odd, 3, odd, odd, ctypes.byref(d), None) == 1
+    assert b"aligned" in lib.paged_kv_last_error()
+    cfg = pkv.DecodeConfig(0, 0)
+    # group of 16 query heads per kv head is outside the supported set
+    assert lib.paged_attention_decode(None, None, None, None, 0, None, 4, 128, 16, 1.0, None, 2, None, 0,
+                                      ctypes.byref(d), ctypes.byref(cfg), None) == 2
+    # workspace too small for a split decode
+    a = ctypes.c_void_p(0x10000)
+    rc = lib.paged_attention_decode(a, a, a, a, 256, a, 4, 32, 4096, 1.0, a, 2, None, 0, ctypes.byref(d),
+                                    ctypes.byref(cfg), None)
+    assert rc == 3, lib.paged_kv_last_error()
+    # too few table columns for the stated max length
+    rc = lib.paged_attention_decode(a, a, a, a, 10, a, 4, 32, 4096, 1.0, a, 2, a, 1 << 30, ctypes.byref(d),
+                                    ctypes.byref(cfg), None)
+    assert rc == 1 and b"max_blocks_per_seq" in lib.paged_kv_last_error()
+    # out dtype f16 for bf16 caches
+    rc = lib.paged_attention_decode(a, a, a, a, 256, a, 4, 32, 4096, 1.0, a, 1, a, 1 << 30, ctypes.byref(d),
+                                    ctypes.byref(cfg), None)
+    assert rc == 2
+
+
+def test_block_copy_pair_checks(lib):
+    d = _desc(num_blocks=10)
+    a = ctypes.c_void_p(0x10000)
+
+    def run(pairs):
+        arr = (ctypes.c_int64 * (2 * len(pairs)))(*[x for p in pairs for x in p])
+        return lib.paged_block_copy(a, arr, len(pairs), a, a, ctypes.byref(d), None)
+
+    assert run([(1, 1)]) == 1                  # onto itself
+    assert run([(1, 2), (3, 2)]) == 1          # destination twice
+    assert run([(1, 2), (2, 3)]) == 1          # destination also a source
+    assert run([(1, 10)]) == 1                 # out of range
+    assert run([(-1, 2)]) == 1
+
+
+def test_binding_fails_loudly_without_a_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    k = torch.zeros(2, 1, 16, 64)
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_kv_append(k[:, 0, :1], k[:, 0, :1], torch.zeros(2, dtype=torch.int64), k, k)

@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bit-exact: append, copy-on-write block copy, block-table gather.  Attention:
+max-abs error <= 1e-5 for f32 inputs and <= 2e-3 for f16/bf16 inputs (fp32
+accumulation), checked with fp32 outputs; with outputs in the input dtype each
+element must also sit within one output ulp of the oracle (|ref| * 2^-8 + 1e-4 for
+bf16, |ref| * 2^-11 + 1e-4 for f16).  Every pool row that should not be read is NaN.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_310_gb300 as pkv
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.float16: 2e-3, torch.bfloat16: 2e-3}
+ULP = {torch.float32: 2.0 ** -22, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+PATHS = [pkv.PATH_CUDA_CORE]
+
+
+def oracle_step(w):
+    kc, vc = w.k_cache.clone(), w.v_cache.clone()
+    oracle.block_copy(w.cow_pairs, kc, vc)
+    oracle.kv_append(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    ref = oracle.attention_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    return ref, kc, vc
+
+
+def gpu_step(w, out_dtype=torch.float32, path=pkv.PATH_AUTO, part=0, g=None):
+    g = g if g is not None else w.to("cuda")
+    if g.cow_pairs.numel():
+        pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache, host_pairs=w.cow_pairs)
+    pkv.paged_kv_append(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+    out = torch.empty(g.q.shape, dtype=out_dtype, device="cuda")
+    pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                               max_context_len=w.max_context_len, path=path, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    return out, g
+
+
+def decode_only(w, g, out_dtype=torch.float32, path=pkv.PATH_AUTO, part=0):
+    out = torch.empty(g.q.shape, dtype=out_dtype, device="cuda")
+    pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                               max_context_len=w.max_context_len, path=path, partition_tokens=part)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    return out
+
+
+def same_bytes(a, b):
+    return torch.equal(a.contiguous().cpu().view(torch.uint8), b.contiguous().cpu().view(torch.uint8))
+
+
+def check_close(out, ref, dtype, in_dtype_out=False):
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert err.max() <= TOL[dtype], f"max-abs error {err.max():.3g} > {TOL[dtype]}"
+    if in_dtype_out:
+        bound = np.abs(ref) * ULP[dtype] + 1e-4
+        bad = err > bound
+        assert not bad.any(), f"{bad.sum()} elements beyond one output ulp (worst {err[bad].max():.3g})"
+    return float(err.max())
+
+
+# ------------------------------------------------------------------------------------
+# the five workloads at full size
+
+_cache = {}
+
+
+def full_case(cfg):
+    if cfg not in _cache:
+        w = workloads.make_workload(cfg)
+        ref, kc, vc = oracle_step(w)
+        _cache.clear()  # keep one large case resident at a time
+        _cache[cfg] = (w, ref, kc, vc)
+    return _cache[cfg]
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("path", PATHS)
+def test_config_parity(cfg, path):
+    w, ref, kc, vc = full_case(cfg)
+    out, g = gpu_step(w, torch.float32, path=path)
+    # append and copy-on-write are bit-exact over the whole pool (NaN payloads included)
+    assert same_bytes(g.k_cache, kc) and same_bytes(g.v_cache, vc)
+    err = check_close(out, ref, w.dtype)
+    print(f"config {cfg} path {path}: max-abs {err:.3g}")
+    if w.dtype != torch.float32:
+        out16 = decode_only(w, g, w.dtype, path=path)
+        check_close(out16, ref, w.dtype, in_dtype_out=True)
+
+
+@pytest.mark.parametrize("cfg", [1, 4])
+def test_config_gather_bit_exact(cfg):
+    w, _, kc, vc = full_case(cfg)
+    g = w.to("cuda")
+    g.k_cache.copy_(kc)
+    g.v_cache.copy_(vc)
+    L = w.max_context_len
+    k_out = torch.zeros((w.num_seqs, w.num_kv_heads, L, w.head_dim), dtype=w.dtype, device="cuda")
+    v_out = torch.zeros_like(k_out)
+    pkv.paged_kv_gather(g.k_cache, g.v_cache, g.block_tables, g.context_lens, k_out, v_out)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    kr, vr = oracle.gather(kc, vc, w.block_tables, w.context_lens, L)
+    assert same_bytes(k_out, kr) and same_bytes(v_out, vr)
+
+
+# ------------------------------------------------------------------------------------
+# small random cases: every dtype, head_dim, block size, group size, partition size
+
+CASES = [
+    # dtype, D, bs, Hq, Hkv, max_len, part
+    ("f32", 64, 16, 4, 4, 40, 0), ("f32", 128, 8, 8, 2, 300, 128), ("f32", 64, 32, 6, 2, 700, 256),
+    ("f16", 128, 16, 8, 1, 1000, 128), ("f16", 64, 8, 3, 3, 260, 0), ("f16", 128, 32, 16, 4, 2000, 384),
+    ("bf16", 128, 16, 32, 4, 900, 256), ("bf16", 64, 16, 5, 1, 129, 128), ("bf16", 128, 8, 7, 7, 513, 0),
+    ("bf16", 128, 32, 64, 8, 1500, 512), ("f16", 128, 16, 2, 1, 3000, 0), ("bf16", 64, 32, 16, 2, 1, 0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-D{c[1]}-bs{c[2]}-{c[3]}x{c[4]}-L{c[5]}-p{c[6]}" for c in CASES])
+@pytest.mark.parametrize("path", PATHS)
+def test_random_parity(case, path):
+    dt, D, bs, Hq, Hkv, max_len, part = case
+    w = workloads.random_workload(310_400 + CASES.index(case), num_seqs=5, max_len=max_len, min_len=1,
+                                  num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs, dtype=dt)
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=path, part=part)
+    assert same_bytes(g.k_cache, kc) and same_bytes(g.v_cache, vc)
+    check_close(out, ref, w.dtype)
+    out2 = decode_only(w, g, w.dtype, path=path, part=part)
+    check_close(out2, ref, w.dtype, in_dtype_out=w.dtype != torch.float32)
+
+
+def test_empty_and_single_token_sequences():
+    w = workloads.random_workload(99, num_seqs=12, max_len=2, min_len=0, num_q_heads=8, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="bf16")
+    assert (w.context_lens == 0).any() and (w.context_lens == 1).any()
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.bfloat16)
+    got = out.cpu()
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        if n == 0:
+            assert (got[s] == 0).all()
+        if n == 1:  # softmax of one score is 1: the output is V_0 exactly
+            b = int(w.block_tables[s, 0])
+            for h in range(w.num_q_heads):
+                assert same_bytes(got[s, h], vc[b, h // 4, 0])
+
+
+# ------------------------------------------------------------------------------------
+# invariants on the GPU
+
+def test_permutation_invariance_bit_exact():
+    w = workloads.random_workload(5, num_seqs=6, max_len=700, min_len=1, num_q_heads=16, num_kv_heads=4,
+                                  head_dim=128, block_size=16, dtype="bf16", canary=False)
+    g = w.to("cuda")
+    base = decode_only(w, g, torch.float32, part=256)
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1))
+    kp, vp = torch.empty_like(w.k_cache), torch.empty_like(w.v_cache)
+    kp[perm] = w.k_cache
+    vp[perm] = w.v_cache
+    bt = w.block_tables.clone()
+    ok = bt >= 0
+    bt[ok] = perm[bt[ok].long()].to(torch.int32)
+    g2 = w.to("cuda")
+    g2.k_cache, g2.v_cache, g2.block_tables = kp.cuda(), vp.cuda(), bt.cuda()
+    moved = decode_only(w, g2, torch.float32, part=256)
+    assert torch.equal(base, moved)
+    again = decode_only(w, g, torch.float32, part=256)
+    assert torch.equal(base, again)  # deterministic
+
+
+def test_shared_vs_copied_bit_exact():
+    w, _, kc, vc = full_case(4)
+    users, nprefix = w.meta["users"], w.meta["prefix_tokens"] // w.block_size
+    g = w.to("cuda")
+    g.k_cache.copy_(kc)
+    g.v_cache.copy_(vc)
+    sel = slice(0, users)
+    sub = workloads.Workload(**{**{k: getattr(w, k) for k in w.__dataclass_fields__},
+                                "context_lens": w.context_lens[sel], "block_tables": w.block_tables[sel],
+                                "q": w.q[sel]})
+    gs = sub.to("cuda")
+    gs.k_cache, gs.v_cache = g.k_cache, g.v_cache
+    shared = decode_only(sub, gs)
+    # private copies of the prefix for users 1..9, made with the library's block copy
+    extra = (users - 1) * nprefix
+    kx = torch.cat([g.k_cache, torch.empty((extra,) + tuple(kc.shape[1:]), dtype=kc.dtype, device="cuda")])
+    vx = torch.cat([g.v_cache, torch.empty_like(kx[:extra])])
+    bt = sub.block_tables.clone()
+    pairs = []
+    for u in range(1, users):
+        for i in range(nprefix):
+            dst = w.num_blocks + (u - 1) * nprefix + i
+            pairs.append((int(bt[u, i]), dst))
+            bt[u, i] = dst
+    pairs = torch.tensor(pairs, dtype=torch.int64)
+    pkv.paged_block_copy(pairs.cuda(), kx, vx, host_pairs=pairs)
+    gs.k_cache, gs.v_cache, gs.block_tables = kx, vx, bt.cuda()
+    copied = decode_only(sub, gs)
+    assert torch.equal(shared, copied)
+
+
+def test_device_flag_on_bad_block_id():
+    w = workloads.random_workload(3, num_seqs=3, max_len=64, min_len=20, num_q_heads=4, num_kv_heads=4,
+                                  head_dim=64, block_size=16, dtype="f16", canary=False)
+    g = w.to("cuda")
+    g.block_tables[1, 0] = w.num_blocks + 5  # the kernel's bounds check turns this into a flag
+    decode_only_out = torch.empty(g.q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale,
+                               decode_only_out, max_context_len=w.max_context_len)
+    assert pkv.device_error() == 5
+    assert pkv.device_error() == 0  # read-and-clear
+    bad = torch.tensor([w.num_blocks * w.block_size + 3], dtype=torch.int64, device="cuda")
+    pkv.paged_kv_append(g.k_new[:1], g.v_new[:1], bad, g.k_cache, g.v_cache)
+    assert pkv.device_error() == 5
+    # a context longer than the host's bound (beyond the partitions it implies) is
+    # reported, not read
+    w2 = workloads.random_workload(8, num_seqs=3, max_len=400, min_len=300, num_q_heads=4, num_kv_heads=4,
+                                   head_dim=64, block_size=16, dtype="f16", canary=False)
+    g2 = w2.to("cuda")
+    out2 = torch.empty(g2.q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_attention_decode(g2.q, g2.k_cache, g2.v_cache, g2.block_tables, g2.context_lens, g2.scale,
+                               out2, max_context_len=100)
+    assert pkv.device_error() == 5
+
+
+def test_binding_rejects_bad_arguments():
+    w = workloads.random_workload(4, num_seqs=2, max_len=20, min_len=1, num_q_heads=4, num_kv_heads=2,
+                                  head_dim=64, block_size=16, dtype="bf16", canary=False)
+    g = w.to("cuda")
+    out = torch.empty(g.q.shape, dtype=torch.float16, device="cuda")
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out)
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_block_copy(torch.tensor([[1, 1]], device="cuda"), g.k_cache, g.v_cache,
+                             host_pairs=torch.tensor([[1, 1]]))
