@@ -2,9 +2,9 @@
 
 Bit-exact: append, copy-on-write block copy, block-table gather.  Attention:
 max-abs error <= 1e-5 for f32 inputs and <= 2e-3 for f16/bf16 inputs (fp32
-accumulation), checked with fp32 outputs; with outputs in the input dtype each
-element must also sit within one output ulp of the oracle (|ref| * 2^-8 + 1e-4 for
-bf16, |ref| * 2^-11 + 1e-4 for f16).  Every pool row that should not be read is NaN.
+accumulation), checked with fp32 outputs; with outputs rounded to the input dtype
+each element must sit within half an output ulp of the oracle plus 1e-4
+(|ref| * 2^-8 + 1e-4 for bf16, |ref| * 2^-11 + 1e-4 for f16).  Every pool row that should not be read is NaN.
 """
 import math
 
@@ -58,14 +58,18 @@ def same_bytes(a, b):
 
 
 def check_close(out, ref, dtype, in_dtype_out=False):
+    """fp32 outputs: max-abs <= TOL.  Outputs rounded to f16/bf16: each element within
+    half an output ulp of the oracle (|ref| * ULP) plus 1e-4 for the fp32 accumulation;
+    a max-abs bound cannot hold there (a bf16 value in [1, 2) has a 3.9e-3 half-ulp)."""
     got = out.cpu().double().numpy()
     assert np.isfinite(got).all()
     err = np.abs(got - ref)
-    assert err.max() <= TOL[dtype], f"max-abs error {err.max():.3g} > {TOL[dtype]}"
     if in_dtype_out:
         bound = np.abs(ref) * ULP[dtype] + 1e-4
         bad = err > bound
-        assert not bad.any(), f"{bad.sum()} elements beyond one output ulp (worst {err[bad].max():.3g})"
+        assert not bad.any(), f"{bad.sum()} elements beyond half an output ulp (worst {err[bad].max():.3g})"
+    else:
+        assert err.max() <= TOL[dtype], f"max-abs error {err.max():.3g} > {TOL[dtype]}"
     return float(err.max())
 
 
