@@ -73,7 +73,7 @@ pkv_status check_cache(const pkv_cache_desc* c) {
 }
 
 struct DecodePlan {
-  int path;         // PKV_PATH_CUDA_CORE (the tensor-core path is added separately)
+  int path;         // PKV_PATH_CUDA_CORE or PKV_PATH_TENSOR_CORE
   int part_tokens;  // tokens per partition, multiple of 128
   int max_parts;    // partitions of the longest sequence
   size_t workspace; // bytes
@@ -90,16 +90,28 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
                 num_q_heads, c->num_kv_heads);
   const int group = num_q_heads / c->num_kv_heads;
-  if (group > 8) return fail(PKV_ERR_UNSUPPORTED, "query-head group %d > 8", group);
   if (max_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len %d < 0", max_len);
-  const int path = cfg ? cfg->path : PKV_PATH_AUTO;
-  if (path != PKV_PATH_AUTO && path != PKV_PATH_CUDA_CORE)
-    return fail(PKV_ERR_UNSUPPORTED, "decode path %d not available", path);
+  int path = cfg ? cfg->path : PKV_PATH_AUTO;
+  if (path < PKV_PATH_AUTO || path > PKV_PATH_TENSOR_CORE)
+    return fail(PKV_ERR_INVALID_ARG, "decode path %d", path);
+  const bool tc_ok = tc_supported(c->dtype, c->head_dim, group, c->block_size);
+  if (path == PKV_PATH_AUTO)  // tensor cores where the query group makes QK and PV real contractions
+    path = tc_ok && group >= 2 ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
+  if (path == PKV_PATH_TENSOR_CORE && !tc_ok)
+    return fail(PKV_ERR_UNSUPPORTED, "tensor-core path needs f16/bf16, head_dim 128, group <= 16 (group %d)",
+                group);
+  if (path == PKV_PATH_CUDA_CORE && group > 8)
+    return fail(PKV_ERR_UNSUPPORTED, "CUDA-core path supports query-head groups <= 8 (group %d)", group);
+  if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * c->block_size > (int64_t{1} << 30))
+    return fail(PKV_ERR_UNSUPPORTED, "pool of %d blocks too large for 32-bit row coordinates", c->num_blocks);
   int part = cfg ? cfg->partition_tokens : 0;
   if (part < 0 || part % 128 || part > 16384)
     return fail(PKV_ERR_INVALID_ARG, "partition_tokens %d: need 0 or a multiple of 128 <= 16384", part);
-  if (part == 0) part = max_len <= 512 ? (max_len < 128 ? 128 : round_up(max_len, 128)) : 512;
-  plan->path = PKV_PATH_CUDA_CORE;
+  if (part == 0) {
+    const int auto_part = path == PKV_PATH_TENSOR_CORE ? 1024 : 512;
+    part = max_len <= auto_part ? (max_len < 128 ? 128 : round_up(max_len, 128)) : auto_part;
+  }
+  plan->path = path;
   plan->part_tokens = part;
   plan->max_parts = max_len == 0 ? 1 : (max_len + part - 1) / part;
   plan->workspace = 0;
@@ -267,7 +279,8 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_simt(p, cache->dtype, s);
+  cudaError_t e = plan.path == PKV_PATH_TENSOR_CORE ? launch_decode_tc(p, cache->dtype, s)
+                                                    : launch_decode_simt(p, cache->dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = launch_merge(p, cache->dtype, s);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");

@@ -1,0 +1,600 @@
+// decode_tc.cu -- tensor-core (tcgen05) paged decode attention for f16/bf16 caches,
+// head_dim 128, up to 16 query heads per KV head.
+//
+// What it computes is the same as the CUDA-core path (note-023, Method/Concepts;
+// "Paged Attention" glossary, paragraph 4 and the GQA paragraph): per sequence s, KV
+// head g and each query head h of g's group, softmax(scale * q_h . K_j) weighted sum
+// of V_j over the tokens j of s, token j read from row j % bs of physical block
+// block_tables[s][j / bs].
+//
+// Why tensor cores: with G query heads per KV head every K/V element feeds 2G
+// multiply-adds.  At G = 8 streaming K/V at HBM speed needs ~64 TFLOP/s, the whole
+// fp32 CUDA-core rate; as two small dense contractions per 128-token chunk it is a
+// few percent of the tensor cores:
+//   S^T[128 tokens x 16] = K[128 x 128 dims] . Q^T[128 x 16]          (QK, M=128 N=16)
+//   O^T[128 dims x 16]   = V^T[128 dims x 128 tokens] . P^T[128 x 16]  (PV, M=128 N=16)
+// The query heads of a group are the N dimension (padded to 16 with unused columns).
+//
+// Persistent CTAs (one per SM, static round-robin over work items = (partition,
+// sequence, KV head)), 192 threads in four roles:
+//  * warp 4, producer: per 128-token chunk, one lane per physical block reads the
+//    block id and issues four tiled TMA loads (K and V, two 64-column halves each,
+//    128-byte swizzle) into a 3-stage ring; blocks past the item's end are loaded
+//    from outside the tensor, which the TMA unit fills with zeros.  It also loads the
+//    item's 16 query rows.
+//  * warp 5, MMA: one lane issues QK for chunk c into S[c%2] (TMEM), then PV for
+//    chunk c-1 into O[(c-1)%2] once its probabilities are in shared memory; commits
+//    release the ring stage and signal the softmax warps.
+//  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
+//    chunk max across the 128 tokens (shuffles + shared memory), online-softmax
+//    rescale, probabilities rounded to the cache dtype into P^T (shared memory), then
+//    read O row t (dimension t) of the previous chunk and accumulate it in registers
+//    with the rescale factor.  The row sum uses the rounded probabilities, so the
+//    output is an exact convex combination of the V rows with those weights.
+//  Rows of the last block past the context end hold real cache data; the softmax
+//  warps zero those V rows in shared memory before PV (a NaN there would survive a
+//  zero weight).
+#include <climits>
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
+constexpr int kStages = 3;
+constexpr int kN = 16;                         // MMA N: query heads per group, padded
+constexpr int kHalf = kChunk * 128;            // one 64-column half of a K or V tile: 16 KB
+constexpr int kStageBytes = 4 * kHalf;         // K lo, K hi, V lo, V hi
+constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 128 B
+constexpr int kPBytes = 2 * kChunk * 16;       // 4 KB: two groups of 8 heads
+constexpr int kOffQ = kStages * kStageBytes;
+constexpr int kOffP = kOffQ + 2 * kQBytes;
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 2 * kStages + 7 * 2 + 1;  // ring (full, empty), 7 pairs, drain
+constexpr int kOffRedMax = kOffBar + kNumBars * 8;
+constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
+constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
+constexpr int kSmemBytes = kOffMisc + 64;
+constexpr uint32_t kTmemCols = 64;             // S[2] at 0/16, O[2] at 32/48
+
+struct Bars {
+  uint64_t* full;   // [kStages] K/V chunk landed (TMA tx)
+  uint64_t* empty;  // [kStages] chunk's MMAs done
+  uint64_t* qfull;  // [2] query tile landed
+  uint64_t* qempty; // [2] QK MMAs of that item done
+  uint64_t* sfull;  // [2] S ready
+  uint64_t* sfree;  // [2] S read by the softmax warps
+  uint64_t* pfull;  // [2] P written
+  uint64_t* ofull;  // [2] O ready
+  uint64_t* ofree;  // [2] O read
+  uint64_t* drain;  // teardown after an abort
+};
+
+__device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  Bars r;
+  r.full = b;
+  r.empty = b + kStages;
+  r.qfull = b + 2 * kStages;
+  r.qempty = r.qfull + 2;
+  r.sfull = r.qempty + 2;
+  r.sfree = r.sfull + 2;
+  r.pfull = r.sfree + 2;
+  r.ofull = r.pfull + 2;
+  r.ofree = r.ofull + 2;
+  r.drain = r.ofree + 2;
+  return r;
+}
+
+struct TcArgs {
+  CUtensorMap tk;  // K pool as [NB*Hkv*bs rows, 128], box 64 x bs, 128-byte swizzle
+  CUtensorMap tv;  // V pool, same
+  CUtensorMap tq;  // q as [S*Hq rows, 128], box 64 x 16
+  DecodeParams p;
+};
+
+// Work item i -> (partition, sequence, kv head); partitions outermost.
+struct Item {
+  int s, g, part, t0, ntok, nchunks, nparts, L;
+};
+
+__device__ __forceinline__ Item decode_item(const DecodeParams& p, int i) {
+  Item it;
+  const int per_part = p.num_seqs * p.num_kv_heads;
+  it.part = i / per_part;
+  const int r = i - it.part * per_part;
+  it.s = r / p.num_kv_heads;
+  it.g = r - it.s * p.num_kv_heads;
+  it.L = p.context_lens[it.s];
+  it.t0 = it.part * p.part_tokens;
+  const bool bad = it.L < 0 || it.L > p.max_parts * p.part_tokens;
+  it.ntok = bad ? 0 : min(p.part_tokens, it.L - it.t0);
+  if (it.ntok < 0) it.ntok = 0;
+  it.nchunks = (it.ntok + kChunk - 1) / kChunk;
+  it.nparts = (it.L + p.part_tokens - 1) / p.part_tokens;
+  return it;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <typename T>
+__device__ __forceinline__ float round_to(float x) {
+  return Elem<T>::to_float(Elem<T>::from_float(x));
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(void* out, size_t i, float x, int out_f32) {
+  if (out_f32)
+    static_cast<float*>(out)[i] = x;
+  else
+    static_cast<T*>(out)[i] = Elem<T>::from_float(x);
+}
+
+template <typename T, int GM>
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const DecodeParams& p = a.p;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const Bars bars = carve_bars(smem);
+  float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);  // [2][4 warps][kN]
+  float* red_l = reinterpret_cast<float*>(smem + kOffRedL);      // [4 warps][kN]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // chunks the producer issued
+  int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // chunks the MMA lane saw land
+  const int G = p.group;
+  const int total_items = p.max_parts * p.num_seqs * p.num_kv_heads;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars.full[i], 1);
+      mbar_init(&bars.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.qfull[i], 1);
+      mbar_init(&bars.qempty[i], 1);
+      mbar_init(&bars.sfull[i], 1);
+      mbar_init(&bars.sfree[i], 4);
+      mbar_init(&bars.pfull[i], 4);
+      mbar_init(&bars.ofull[i], 1);
+      mbar_init(&bars.ofree[i], 4);
+    }
+    *abort_flag = 0;
+    *issued_slot = 0;
+    *waited_slot = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      prefetch_tensormap(&a.tk);
+      prefetch_tensormap(&a.tv);
+      prefetch_tensormap(&a.tq);
+    }
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    const int bs = p.block_size;
+    const int blocks_per_chunk = kChunk / bs;
+    const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row outside the pool
+    int c = 0, j = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
+      const Item it = decode_item(p, i);
+      if (it.ntok <= 0) continue;
+      const int qb = j & 1;
+      if (lane == 0) {
+        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
+          unsigned char* qdst = smem + kOffQ + qb * kQBytes;
+          const int qrow = it.s * p.num_q_heads + it.g * G;
+          tma_load_2d(qdst, &a.tq, 0, qrow, &bars.qfull[qb], pol_keep);
+          tma_load_2d(qdst + kQBytes / 2, &a.tq, 64, qrow, &bars.qfull[qb], pol_keep);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
+      for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
+        const int st = c % kStages;
+        if (lane == 0) {
+          ok = c < kStages || wait_role(&bars.empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        __syncwarp();
+        if (lane < blocks_per_chunk) {
+          const int lb = it.t0 / bs + k * blocks_per_chunk + lane;  // logical block
+          int row = oob_row;
+          if (lb * bs < it.t0 + it.ntok) {
+            int b = lb < p.max_blocks_per_seq ? table[lb] : -1;
+            if (b < 0 || b >= p.num_blocks) {
+              set_error(p.err, kErrIndex);
+              b = 0;
+            }
+            row = (b * p.num_kv_heads + it.g) * bs;
+          }
+          unsigned char* dst = smem + st * kStageBytes + lane * bs * 128;
+          tma_load_2d(dst, &a.tk, 0, row, &bars.full[st], pol_stream);
+          tma_load_2d(dst + kHalf, &a.tk, 64, row, &bars.full[st], pol_stream);
+          tma_load_2d(dst + 2 * kHalf, &a.tv, 0, row, &bars.full[st], pol_stream);
+          tma_load_2d(dst + 3 * kHalf, &a.tv, 64, row, &bars.full[st], pol_stream);
+        }
+        if (lane == 0) *issued_slot = c + 1;
+      }
+      ++j;
+    }
+  } else if (warp == 5) {
+    // ============================ MMA issuer ============================
+    if (lane == 0) {
+      constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+      constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
+      constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, kN);
+      const uint32_t ring = smem_addr(smem);
+      const uint32_t qbase = smem_addr(smem + kOffQ);
+      const uint32_t pbase = smem_addr(smem + kOffP);
+      int c = 0, j = 0;
+      bool ok = true;
+      auto issue_pv = [&](int cp) -> bool {
+        const int pb = cp & 1, st = cp % kStages;
+        if (!wait_role(&bars.pfull[pb], (cp >> 1) & 1, abort_flag, p.err)) return false;
+        if (cp >= 2 && !wait_role(&bars.ofree[pb], ((cp >> 1) - 1) & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t vbase = ring + st * kStageBytes + 2 * kHalf;
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+          const uint64_t ad = smem_desc(vbase + kk * 2048, kHalf, 1024, kLayoutSwizzle128);
+          const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
+          mma_f16(tmem + 32 + pb * 16, ad, bd, idesc_pv, kk > 0);
+        }
+        mma_commit(&bars.ofull[pb]);
+        mma_commit(&bars.empty[st]);
+        return true;
+      };
+      for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
+        const Item it = decode_item(p, i);
+        if (it.ntok <= 0) continue;
+        const int qb = j & 1;
+        for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
+          const int st = c % kStages, sb = c & 1;
+          ok = (k > 0 || wait_role(&bars.qfull[qb], (j >> 1) & 1, abort_flag, p.err)) &&
+               wait_role(&bars.full[st], (c / kStages) & 1, abort_flag, p.err) &&
+               (c < 2 || wait_role(&bars.sfree[sb], ((c >> 1) - 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          *waited_slot = c + 1;
+          tc_fence_after();
+          const uint32_t kb = ring + st * kStageBytes;
+          const uint32_t qa = qbase + qb * kQBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kLayoutSwizzle128);
+            const uint64_t bd = smem_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024,
+                                          kLayoutSwizzle128);
+            mma_f16(tmem + sb * 16, ad, bd, idesc_qk, kk > 0);
+          }
+          mma_commit(&bars.sfull[sb]);
+          if (k == it.nchunks - 1) mma_commit(&bars.qempty[qb]);
+          if (c >= 1 && !issue_pv(c - 1)) ok = false;
+        }
+        ++j;
+      }
+      if (ok && c >= 1) issue_pv(c - 1);
+    }
+    __syncwarp();
+  } else {
+    // ============================ softmax warps ============================
+    const int t = threadIdx.x;  // TMEM lane: token row of S, dimension row of O
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m[GM], lp[GM], alpha[GM], alpha_pend[GM], acc[GM], Lcur[GM], Mcur[GM], Lpend[GM], Mpend[GM];
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+      m[h] = -INFINITY; lp[h] = 0.f; alpha[h] = 0.f; alpha_pend[h] = 0.f; acc[h] = 0.f;
+      Lcur[h] = 1.f; Mcur[h] = 0.f; Lpend[h] = 1.f; Mpend[h] = 0.f;
+    }
+    // pending chunk (its O not yet consumed): item fields and flags
+    int pend_s = 0, pend_g = 0, pend_part = 0, pend_nparts = 0;
+    bool pend_first = false, pend_last = false;
+    int c = 0;
+    bool ok = true;
+
+    // Returns false (warp-uniform) when the wait for O ran out or another role aborted;
+    // the caller then stops at the next collective barrier.
+    auto consume = [&](int cp) -> bool {
+      const int pb = cp & 1;
+      if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err)))
+        return false;
+      tc_fence_after();
+      float o[16];
+      tmem_load16(lane_base + 32 + pb * 16, o);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ofree[pb]);
+#pragma unroll
+      for (int h = 0; h < GM; ++h) acc[h] = pend_first ? o[h] : fmaf(acc[h], alpha_pend[h], o[h]);
+      if (pend_last) {
+        const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G;
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          if (h < G) {
+            const size_t row = row0 + h;
+            if (pend_nparts == 1) {
+              store_out<T>(p.out, row * 128 + t, acc[h] / Lpend[h], p.out_f32);
+            } else {
+              const size_t k = row * p.max_parts + pend_part;
+              p.ws_o[k * 128 + t] = acc[h];
+              if (t == 0) {
+                p.ws_ml[2 * k] = Mpend[h];
+                p.ws_ml[2 * k + 1] = Lpend[h];
+              }
+            }
+          }
+        }
+      }
+      return true;
+    };
+
+    bool prev_ok = true;  // outcome of the last consume (warp-uniform)
+    for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
+      const Item it = decode_item(p, i);
+      if (it.part == 0 && (it.L < 0 || it.L > p.max_parts * p.part_tokens)) {
+        if (t == 0) set_error(p.err, kErrLength);
+        continue;
+      }
+      if (it.L == 0 && it.part == 0) {  // empty context: the neutral output, no MMA work
+        for (int h = 0; h < G; ++h)
+          store_out<T>(p.out, (static_cast<size_t>(it.s) * p.num_q_heads + it.g * G + h) * 128 + t, 0.f,
+                       p.out_f32);
+        continue;
+      }
+      if (it.ntok <= 0) continue;
+#pragma unroll
+      for (int h = 0; h < GM; ++h) {
+        m[h] = -INFINITY;
+        lp[h] = 0.f;
+      }
+      for (int k = 0; k < it.nchunks; ++k, ++c) {
+        const int sb = c & 1;
+        const bool wok = __all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err));
+        float sv[16];
+        if (wok) {
+          tc_fence_after();
+          tmem_load16(lane_base + sb * 16, sv);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.sfree[sb]);
+        }
+        const int rows_valid = min(kChunk, it.ntok - k * kChunk);
+        const bool valid = wok && t < rows_valid;
+        // chunk max over the 128 tokens, per head
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
+          float v = sv[h];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+          if (lane == 0) red_max[(sb * 4 + warp) * kN + h] = v;
+        }
+        // every softmax warp learns whether all four got here normally
+        if (!named_barrier_and(1, 128, wok && prev_ok)) {
+          ok = false;
+          break;
+        }
+        float pr[16];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          const float* r = red_max + sb * 4 * kN + h;
+          const float cm = fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN]));
+          const float mn = fmaxf(m[h], cm);
+          alpha[h] = exp2f(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
+          m[h] = mn;
+          pr[h] = h < G ? round_to<T>(exp2f(sv[h] - mn)) : 0.f;
+          lp[h] = fmaf(lp[h], alpha[h], pr[h]);
+        }
+#pragma unroll
+        for (int h = GM; h < 16; ++h) pr[h] = 0.f;
+        // P^T for PV: token t's 16 head weights, MN-major without swizzle
+        unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
+        *reinterpret_cast<uint4*>(pdst) = make_uint4(pack2<T>(pr[0], pr[1]), pack2<T>(pr[2], pr[3]),
+                                                     pack2<T>(pr[4], pr[5]), pack2<T>(pr[6], pr[7]));
+        *reinterpret_cast<uint4*>(pdst + kChunk * 16) =
+            make_uint4(pack2<T>(pr[8], pr[9]), pack2<T>(pr[10], pr[11]), pack2<T>(pr[12], pr[13]),
+                       pack2<T>(pr[14], pr[15]));
+        // rows of the last loaded block past the context end: zero their V rows
+        const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
+        if (t >= rows_valid && t < rows_loaded) {
+          unsigned char* vrow = smem + (c % kStages) * kStageBytes + 2 * kHalf + t * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(vrow + kHalf)[q] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.pfull[sb]);
+
+        const bool last = k == it.nchunks - 1;
+        if (last) {  // totals of this item (row sums over the 128 lanes)
+#pragma unroll
+          for (int h = 0; h < GM; ++h) {
+            float v = lp[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) red_l[warp * kN + h] = v;
+          }
+          named_barrier_sync(1, 128);
+#pragma unroll
+          for (int h = 0; h < GM; ++h) {
+            Lcur[h] = (red_l[h] + red_l[kN + h]) + (red_l[2 * kN + h] + red_l[3 * kN + h]);
+            Mcur[h] = m[h];
+          }
+        }
+        if (c >= 1) prev_ok = consume(c - 1);
+        // chunk c becomes the pending one
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+          alpha_pend[h] = alpha[h];
+          if (last) {
+            Lpend[h] = Lcur[h];
+            Mpend[h] = Mcur[h];
+          }
+        }
+        pend_first = k == 0;
+        pend_last = last;
+        pend_s = it.s;
+        pend_g = it.g;
+        pend_part = it.part;
+        pend_nparts = it.nparts;
+      }
+    }
+    if (ok && prev_ok && c >= 1) consume(c - 1);
+    __syncwarp();
+  }
+
+  // ---------------- teardown ----------------
+  __syncthreads();
+  if (*abort_flag) {
+    // a wait ran out: let in-flight copies and MMAs finish (bounded) before leaving
+    if (warp == 4 && lane == 0) {
+      for (int c = *waited_slot; c < *issued_slot; ++c)
+        if (!mbar_wait(&bars.full[c % kStages], (c / kStages) & 1)) break;
+    }
+    if (warp == 5 && lane == 0) {
+      mbar_init(bars.drain, 1);
+      fence_barrier_init();
+      mma_commit(bars.drain);
+      mbar_wait(bars.drain, 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D map over rows of 128 16-bit elements, box 64 x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <typename T, int GM>
+cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, GM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  decode_tc_kernel<T, GM><<<grid, kThreads, kSmemBytes, stream>>>(args);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_tc_g(const TcArgs& args, int grid, cudaStream_t stream) {
+  const int G = args.p.group;
+  if (G <= 1) return launch_tc_t<T, 1>(args, grid, stream);
+  if (G <= 2) return launch_tc_t<T, 2>(args, grid, stream);
+  if (G <= 4) return launch_tc_t<T, 4>(args, grid, stream);
+  if (G <= 8) return launch_tc_t<T, 8>(args, grid, stream);
+  return launch_tc_t<T, 16>(args, grid, stream);
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int head_dim, int group, int block_size) {
+  return (dtype == PKV_F16 || dtype == PKV_BF16) && head_dim == 128 && group >= 1 && group <= kN &&
+         (block_size == 8 || block_size == 16 || block_size == 32);
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream) {
+  TcArgs args;
+  args.p = p;
+  const bool bf16 = dtype == PKV_BF16;
+  const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
+  if (!make_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
+      !make_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
+      !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16))
+    return cudaErrorInvalidValue;
+  const int items = p.max_parts * p.num_seqs * p.num_kv_heads;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = items < sms ? items : sms;
+  if (grid == 0) return cudaSuccess;
+  return bf16 ? launch_tc_g<__nv_bfloat16>(args, grid, stream) : launch_tc_g<__half>(args, grid, stream);
+}
+
+}  // namespace pkv

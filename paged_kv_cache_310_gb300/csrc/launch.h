@@ -28,6 +28,9 @@ struct DecodeParams {
 
 // CUDA-core split-K decode (any supported dtype, head_dim 64/128, group <= 8).
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t stream);
+// Tensor-core (tcgen05) decode: f16/bf16, head_dim 128, group <= 16, persistent CTAs.
+bool tc_supported(int dtype, int head_dim, int group, int block_size);
+cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Partition merge for sequences longer than one partition.
 cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
 

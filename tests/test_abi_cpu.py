@@ -45,13 +45,18 @@ def _ws(lib, S, Hq, L, desc, part=0, path=0):
 
 def test_workspace_sizes(lib):
     d = _desc()
-    assert _ws(lib, 64, 32, 512, d) == 0            # one partition: no workspace
-    n = _ws(lib, 64, 32, 2048, d)                   # 4 partitions of 512
+    core, tensor = pkv.PATH_CUDA_CORE, pkv.PATH_TENSOR_CORE
+    assert _ws(lib, 64, 32, 512, d, path=core) == 0      # one partition: no workspace
+    n = _ws(lib, 64, 32, 2048, d, path=core)             # 4 partitions of 512
     rows = 64 * 32 * 4
     assert n == -(-rows * 8 // 256) * 256 + rows * 128 * 4
-    assert _ws(lib, 64, 32, 2048, d, part=1024) < n
-    assert _ws(lib, 64, 32, 2048, d, part=100) == 0  # invalid partition size
-    assert _ws(lib, 64, 30, 2048, d) == 0            # heads not a multiple of kv heads
+    assert _ws(lib, 64, 32, 2048, d, part=1024, path=core) < n
+    # the tensor-core path (chosen automatically for groups >= 2) splits at 1024 tokens
+    assert _ws(lib, 64, 32, 2048, d) == _ws(lib, 64, 32, 2048, d, path=tensor)
+    assert _ws(lib, 64, 32, 1024, d, path=tensor) == 0
+    assert _ws(lib, 64, 32, 2048, d, part=100) == 0       # invalid partition size
+    assert _ws(lib, 64, 30, 2048, d) == 0                 # heads not a multiple of kv heads
+    assert _ws(lib, 4, 8, 2048, _desc(dtype=pkv.F32), path=tensor) == 0  # f32 has no tensor path
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -75,9 +80,12 @@ def test_argument_checks_before_device_work(lib):
     assert lib.paged_kv_append(odd, odd, odd, 3, odd, odd, ctypes.byref(d), None) == 1
     assert b"aligned" in lib.paged_kv_last_error()
     cfg = pkv.DecodeConfig(0, 0)
-    # group of 16 query heads per kv head is outside the supported set
-    assert lib.paged_attention_decode(None, None, None, None, 0, None, 4, 128, 16, 1.0, None, 2, None, 0,
+    # a group of 17 query heads per kv head is outside the supported set; 16 only on tensor cores
+    assert lib.paged_attention_decode(None, None, None, None, 0, None, 4, 136, 16, 1.0, None, 2, None, 0,
                                       ctypes.byref(d), ctypes.byref(cfg), None) == 2
+    core = pkv.DecodeConfig(pkv.PATH_CUDA_CORE, 0)
+    assert lib.paged_attention_decode(None, None, None, None, 0, None, 4, 128, 16, 1.0, None, 2, None, 0,
+                                      ctypes.byref(d), ctypes.byref(core), None) == 2
     # workspace too small for a split decode
     a = ctypes.c_void_p(0x10000)
     rc = lib.paged_attention_decode(a, a, a, a, 256, a, 4, 32, 4096, 1.0, a, 2, None, 0, ctypes.byref(d),

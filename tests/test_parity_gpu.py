@@ -20,7 +20,15 @@ pytestmark = pytest.mark.gpu
 
 TOL = {torch.float32: 1e-5, torch.float16: 2e-3, torch.bfloat16: 2e-3}
 ULP = {torch.float32: 2.0 ** -22, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
-PATHS = [pkv.PATH_CUDA_CORE]
+PATHS = [pkv.PATH_CUDA_CORE, pkv.PATH_TENSOR_CORE]
+PATH_IDS = {pkv.PATH_CUDA_CORE: "cuda_core", pkv.PATH_TENSOR_CORE: "tensor_core"}
+
+
+def supported(path, dtype, head_dim, group):
+    """The library's supported set per path (include/pagedkv.h)."""
+    if path == pkv.PATH_TENSOR_CORE:
+        return dtype in (torch.float16, torch.bfloat16) and head_dim == 128 and group <= 16
+    return group <= 8
 
 
 def oracle_step(w):
@@ -89,9 +97,11 @@ def full_case(cfg):
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
 def test_config_parity(cfg, path):
     w, ref, kc, vc = full_case(cfg)
+    if not supported(path, w.dtype, w.head_dim, w.num_q_heads // w.num_kv_heads):
+        pytest.skip("outside this path's supported set")
     out, g = gpu_step(w, torch.float32, path=path)
     # append and copy-on-write are bit-exact over the whole pool (NaN payloads included)
     assert same_bytes(g.k_cache, kc) and same_bytes(g.v_cache, vc)
@@ -127,13 +137,17 @@ CASES = [
     ("f16", 128, 16, 8, 1, 1000, 128), ("f16", 64, 8, 3, 3, 260, 0), ("f16", 128, 32, 16, 4, 2000, 384),
     ("bf16", 128, 16, 32, 4, 900, 256), ("bf16", 64, 16, 5, 1, 129, 128), ("bf16", 128, 8, 7, 7, 513, 0),
     ("bf16", 128, 32, 64, 8, 1500, 512), ("f16", 128, 16, 2, 1, 3000, 0), ("bf16", 64, 32, 16, 2, 1, 0),
+    ("bf16", 128, 16, 48, 4, 700, 0), ("f16", 128, 8, 32, 2, 1200, 128), ("bf16", 128, 16, 1, 1, 2500, 256),
+    ("f16", 128, 32, 4, 4, 200, 0), ("bf16", 128, 8, 24, 8, 3000, 384),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-D{c[1]}-bs{c[2]}-{c[3]}x{c[4]}-L{c[5]}-p{c[6]}" for c in CASES])
-@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
 def test_random_parity(case, path):
     dt, D, bs, Hq, Hkv, max_len, part = case
+    if not supported(path, workloads.DTYPES[dt], D, Hq // Hkv):
+        pytest.skip("outside this path's supported set")
     w = workloads.random_workload(310_400 + CASES.index(case), num_seqs=5, max_len=max_len, min_len=1,
                                   num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs, dtype=dt)
     ref, kc, vc = oracle_step(w)
@@ -144,12 +158,13 @@ def test_random_parity(case, path):
     check_close(out2, ref, w.dtype, in_dtype_out=w.dtype != torch.float32)
 
 
-def test_empty_and_single_token_sequences():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_empty_and_single_token_sequences(path):
     w = workloads.random_workload(99, num_seqs=12, max_len=2, min_len=0, num_q_heads=8, num_kv_heads=2,
                                   head_dim=128, block_size=16, dtype="bf16")
     assert (w.context_lens == 0).any() and (w.context_lens == 1).any()
     ref, kc, vc = oracle_step(w)
-    out, g = gpu_step(w, torch.bfloat16)
+    out, g = gpu_step(w, torch.bfloat16, path=path)
     got = out.cpu()
     for s in range(w.num_seqs):
         n = int(w.context_lens[s])
@@ -164,11 +179,12 @@ def test_empty_and_single_token_sequences():
 # ------------------------------------------------------------------------------------
 # invariants on the GPU
 
-def test_permutation_invariance_bit_exact():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_permutation_invariance_bit_exact(path):
     w = workloads.random_workload(5, num_seqs=6, max_len=700, min_len=1, num_q_heads=16, num_kv_heads=4,
                                   head_dim=128, block_size=16, dtype="bf16", canary=False)
     g = w.to("cuda")
-    base = decode_only(w, g, torch.float32, part=256)
+    base = decode_only(w, g, torch.float32, path=path, part=256)
     perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1))
     kp, vp = torch.empty_like(w.k_cache), torch.empty_like(w.v_cache)
     kp[perm] = w.k_cache
@@ -178,13 +194,14 @@ def test_permutation_invariance_bit_exact():
     bt[ok] = perm[bt[ok].long()].to(torch.int32)
     g2 = w.to("cuda")
     g2.k_cache, g2.v_cache, g2.block_tables = kp.cuda(), vp.cuda(), bt.cuda()
-    moved = decode_only(w, g2, torch.float32, part=256)
+    moved = decode_only(w, g2, torch.float32, path=path, part=256)
     assert torch.equal(base, moved)
-    again = decode_only(w, g, torch.float32, part=256)
+    again = decode_only(w, g, torch.float32, path=path, part=256)
     assert torch.equal(base, again)  # deterministic
 
 
-def test_shared_vs_copied_bit_exact():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_shared_vs_copied_bit_exact(path):
     w, _, kc, vc = full_case(4)
     users, nprefix = w.meta["users"], w.meta["prefix_tokens"] // w.block_size
     g = w.to("cuda")
@@ -196,7 +213,7 @@ def test_shared_vs_copied_bit_exact():
                                 "q": w.q[sel]})
     gs = sub.to("cuda")
     gs.k_cache, gs.v_cache = g.k_cache, g.v_cache
-    shared = decode_only(sub, gs)
+    shared = decode_only(sub, gs, path=path)
     # private copies of the prefix for users 1..9, made with the library's block copy
     extra = (users - 1) * nprefix
     kx = torch.cat([g.k_cache, torch.empty((extra,) + tuple(kc.shape[1:]), dtype=kc.dtype, device="cuda")])
@@ -211,18 +228,19 @@ def test_shared_vs_copied_bit_exact():
     pairs = torch.tensor(pairs, dtype=torch.int64)
     pkv.paged_block_copy(pairs.cuda(), kx, vx, host_pairs=pairs)
     gs.k_cache, gs.v_cache, gs.block_tables = kx, vx, bt.cuda()
-    copied = decode_only(sub, gs)
+    copied = decode_only(sub, gs, path=path)
     assert torch.equal(shared, copied)
 
 
-def test_device_flag_on_bad_block_id():
-    w = workloads.random_workload(3, num_seqs=3, max_len=64, min_len=20, num_q_heads=4, num_kv_heads=4,
-                                  head_dim=64, block_size=16, dtype="f16", canary=False)
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_device_flag_on_bad_block_id(path):
+    w = workloads.random_workload(3, num_seqs=3, max_len=64, min_len=20, num_q_heads=4, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="f16", canary=False)
     g = w.to("cuda")
     g.block_tables[1, 0] = w.num_blocks + 5  # the kernel's bounds check turns this into a flag
     decode_only_out = torch.empty(g.q.shape, dtype=torch.float32, device="cuda")
     pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale,
-                               decode_only_out, max_context_len=w.max_context_len)
+                               decode_only_out, max_context_len=w.max_context_len, path=path)
     assert pkv.device_error() == 5
     assert pkv.device_error() == 0  # read-and-clear
     bad = torch.tensor([w.num_blocks * w.block_size + 3], dtype=torch.int64, device="cuda")
@@ -230,12 +248,12 @@ def test_device_flag_on_bad_block_id():
     assert pkv.device_error() == 5
     # a context longer than the host's bound (beyond the partitions it implies) is
     # reported, not read
-    w2 = workloads.random_workload(8, num_seqs=3, max_len=400, min_len=300, num_q_heads=4, num_kv_heads=4,
-                                   head_dim=64, block_size=16, dtype="f16", canary=False)
+    w2 = workloads.random_workload(8, num_seqs=3, max_len=400, min_len=300, num_q_heads=4, num_kv_heads=2,
+                                   head_dim=128, block_size=16, dtype="f16", canary=False)
     g2 = w2.to("cuda")
     out2 = torch.empty(g2.q.shape, dtype=torch.float32, device="cuda")
     pkv.paged_attention_decode(g2.q, g2.k_cache, g2.v_cache, g2.block_tables, g2.context_lens, g2.scale,
-                               out2, max_context_len=100)
+                               out2, max_context_len=100, path=path)
     assert pkv.device_error() == 5
 
 
