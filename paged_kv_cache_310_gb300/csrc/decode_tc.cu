@@ -18,13 +18,15 @@
 // Persistent CTAs (one per SM, static round-robin over work items = (partition,
 // sequence, KV head)), 192 threads in four roles:
 //  * warp 4, producer: per 128-token chunk, one lane per physical block reads the
-//    block id and issues four tiled TMA loads (K and V, two 64-column halves each,
+//    block id (before waiting for a free stage, hiding its latency) and issues four
+//    tiled TMA loads (K and V, two 64-column halves each,
 //    128-byte swizzle) into a 3-stage ring; blocks past the item's end are loaded
 //    from outside the tensor, which the TMA unit fills with zeros.  It also loads the
 //    item's 16 query rows.
-//  * warp 5, MMA: one lane issues QK for chunk c into S[c%2] (TMEM), then PV for
-//    chunk c-1 into O[(c-1)%2] once its probabilities are in shared memory; commits
-//    release the ring stage and signal the softmax warps.
+//  * warp 5, MMA: one lane polls and issues QK for chunk c into S[c%2] (TMEM) as
+//    soon as its K/V landed, and PV for chunk c into O[c%2] as soon as its
+//    probabilities are in shared memory; commits release the ring stage and signal
+//    the softmax warps.
 //  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
 //    chunk max across the 128 tokens (shuffles + shared memory), online-softmax
 //    rescale, probabilities rounded to the cache dtype into P^T (shared memory), then
@@ -235,6 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
         const int st = c % kStages;
+        // block ids first: their latency overlaps the wait for a free stage
+        const int lb = it.t0 / bs + k * blocks_per_chunk + lane;  // logical block of this lane
+        const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
+        int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
           ok = c < kStages || wait_role(&bars.empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
           if (ok) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
@@ -243,10 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (!ok) break;
         __syncwarp();
         if (lane < blocks_per_chunk) {
-          const int lb = it.t0 / bs + k * blocks_per_chunk + lane;  // logical block
-          int row = oob_row;
-          if (lb * bs < it.t0 + it.ntok) {
-            int b = lb < p.max_blocks_per_seq ? table[lb] : -1;
+          int row = oob_row;  // blocks past the item's end: zero-filled by the TMA unit
+          if (live) {
             if (b < 0 || b >= p.num_blocks) {
               set_error(p.err, kErrIndex);
               b = 0;
@@ -265,6 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ============================
+    // One lane polls both streams and issues whichever is ready: QK of the next chunk
+    // (its K/V landed, its S buffer free) or PV of the oldest chunk whose
+    // probabilities are written.  Neither waits behind the other.
     if (lane == 0) {
       constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
       constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
@@ -272,52 +279,80 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const uint32_t ring = smem_addr(smem);
       const uint32_t qbase = smem_addr(smem + kOffQ);
       const uint32_t pbase = smem_addr(smem + kOffP);
-      int c = 0, j = 0;
-      bool ok = true;
-      auto issue_pv = [&](int cp) -> bool {
-        const int pb = cp & 1, st = cp % kStages;
-        if (!wait_role(&bars.pfull[pb], (cp >> 1) & 1, abort_flag, p.err)) return false;
-        if (cp >= 2 && !wait_role(&bars.ofree[pb], ((cp >> 1) - 1) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t vbase = ring + st * kStageBytes + 2 * kHalf;
-#pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk) {
-          const uint64_t ad = smem_desc(vbase + kk * 2048, kHalf, 1024, kLayoutSwizzle128);
-          const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
-          mma_f16(tmem + 32 + pb * 16, ad, bd, idesc_pv, kk > 0);
-        }
-        mma_commit(&bars.ofull[pb]);
-        mma_commit(&bars.empty[st]);
-        return true;
-      };
-      for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
-        const Item it = decode_item(p, i);
-        if (it.ntok <= 0) continue;
-        const int qb = j & 1;
-        for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
-          const int st = c % kStages, sb = c & 1;
-          ok = (k > 0 || wait_role(&bars.qfull[qb], (j >> 1) & 1, abort_flag, p.err)) &&
-               wait_role(&bars.full[st], (c / kStages) & 1, abort_flag, p.err) &&
-               (c < 2 || wait_role(&bars.sfree[sb], ((c >> 1) - 1) & 1, abort_flag, p.err));
-          if (!ok) break;
-          *waited_slot = c + 1;
-          tc_fence_after();
-          const uint32_t kb = ring + st * kStageBytes;
-          const uint32_t qa = qbase + qb * kQBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kLayoutSwizzle128);
-            const uint64_t bd = smem_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024,
-                                          kLayoutSwizzle128);
-            mma_f16(tmem + sb * 16, ad, bd, idesc_qk, kk > 0);
+      // QK cursor: item index, chunk within it, items started, chunks in the item
+      int qi = blockIdx.x, qk = 0, qj = 0, qn = 0;
+      auto next_item = [&]() {
+        for (; qi < total_items; qi += gridDim.x) {
+          const Item it = decode_item(p, qi);
+          if (it.ntok > 0) {
+            qn = it.nchunks;
+            return;
           }
-          mma_commit(&bars.sfull[sb]);
-          if (k == it.nchunks - 1) mma_commit(&bars.qempty[qb]);
-          if (c >= 1 && !issue_pv(c - 1)) ok = false;
         }
-        ++j;
+        qn = 0;
+      };
+      next_item();
+      int qc = 0, pc = 0;  // next chunk to QK, next chunk to PV
+      uint64_t idle_since = global_timer_ns();
+      while (qi < total_items || pc < qc) {
+        bool progressed = false;
+        if (qi < total_items) {
+          const int st = qc % kStages, sb = qc & 1, qb = qj & 1;
+          if ((qk > 0 || mbar_try_wait(&bars.qfull[qb], (qj >> 1) & 1)) &&
+              mbar_try_wait(&bars.full[st], (qc / kStages) & 1) &&
+              (qc < 2 || mbar_try_wait(&bars.sfree[sb], ((qc >> 1) - 1) & 1))) {
+            *waited_slot = qc + 1;
+            tc_fence_after();
+            const uint32_t kb = ring + st * kStageBytes;
+            const uint32_t qa = qbase + qb * kQBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kLayoutSwizzle128);
+              const uint64_t bd = smem_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024,
+                                            kLayoutSwizzle128);
+              mma_f16(tmem + sb * 16, ad, bd, idesc_qk, kk > 0);
+            }
+            mma_commit(&bars.sfull[sb]);
+            ++qc;
+            if (++qk == qn) {  // the item's last QK: its query buffer can be refilled
+              mma_commit(&bars.qempty[qb]);
+              qk = 0;
+              ++qj;
+              qi += gridDim.x;
+              next_item();
+            }
+            progressed = true;
+          }
+        }
+        if (pc < qc) {
+          const int pb = pc & 1, st = pc % kStages;
+          if (mbar_try_wait(&bars.pfull[pb], (pc >> 1) & 1) &&
+              (pc < 2 || mbar_try_wait(&bars.ofree[pb], ((pc >> 1) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t vbase = ring + st * kStageBytes + 2 * kHalf;
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk) {
+              const uint64_t ad = smem_desc(vbase + kk * 2048, kHalf, 1024, kLayoutSwizzle128);
+              const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
+              mma_f16(tmem + 32 + pb * 16, ad, bd, idesc_pv, kk > 0);
+            }
+            mma_commit(&bars.ofull[pb]);
+            mma_commit(&bars.empty[st]);
+            ++pc;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = global_timer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (global_timer_ns() - idle_since > kWaitLimitNs) {
+            *abort_flag = 1;
+            set_error(p.err, kErrTimeout);
+            break;
+          }
+        }
       }
-      if (ok && c >= 1) issue_pv(c - 1);
     }
     __syncwarp();
   } else {
