@@ -120,8 +120,10 @@ pkv_status paged_block_copy(const int64_t* src_dst_pairs, const int64_t* host_pa
                             const pkv_cache_desc* cache, void* stream);
 
 /*
- * Bytes of workspace paged_attention_decode needs for these sizes and config
- * (0 when every sequence fits one partition).  max_context_len: host upper bound on
+ * Bytes of workspace paged_attention_decode needs for these sizes and config.  The
+ * CUDA-core path needs none when every sequence fits one partition; the tensor-core
+ * path always needs room for its work list (16 bytes per (sequence, KV head,
+ * partition) plus 256) and, past one partition, the partition partials.  max_context_len: host upper bound on
  * context_lens.  Returns 0 for invalid arguments as well (then the decode call
  * itself reports the error).
  */

@@ -77,6 +77,8 @@ struct DecodePlan {
   int part_tokens;  // tokens per partition, multiple of 128
   int max_parts;    // partitions of the longest sequence
   size_t workspace; // bytes
+  size_t list_bytes;  // work list (tensor-core path): 256-byte header + entries
+  size_t ml_bytes;    // partition (max, sum) pairs
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -107,6 +109,9 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   int part = cfg ? cfg->partition_tokens : 0;
   if (part < 0 || part % 128 || part > 16384)
     return fail(PKV_ERR_INVALID_ARG, "partition_tokens %d: need 0 or a multiple of 128 <= 16384", part);
+  if (path == PKV_PATH_TENSOR_CORE && part > kTcMaxPartition)
+    return fail(PKV_ERR_INVALID_ARG, "tensor-core partitions are at most %d tokens (%d asked)",
+                kTcMaxPartition, part);
   if (part == 0) {
     const int auto_part = path == PKV_PATH_TENSOR_CORE ? 1024 : 512;
     part = max_len <= auto_part ? (max_len < 128 ? 128 : round_up(max_len, 128)) : auto_part;
@@ -114,11 +119,22 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   plan->path = path;
   plan->part_tokens = part;
   plan->max_parts = max_len == 0 ? 1 : (max_len + part - 1) / part;
-  plan->workspace = 0;
+  if (path == PKV_PATH_TENSOR_CORE && plan->max_parts >= 32768)
+    return fail(PKV_ERR_UNSUPPORTED, "tensor-core path: %d partitions per sequence is too many", plan->max_parts);
+  if (static_cast<int64_t>(plan->max_parts) * num_seqs * c->num_kv_heads > (int64_t{1} << 30))
+    return fail(PKV_ERR_UNSUPPORTED, "too many (partition, sequence, kv head) items");
+  // layout: [work list header + entries (tensor-core path)] [partition (max, sum)] [partition outputs]
+  plan->list_bytes = 0;
+  if (path == PKV_PATH_TENSOR_CORE) {
+    const size_t entries = static_cast<size_t>(plan->max_parts) * num_seqs * c->num_kv_heads;
+    plan->list_bytes = 256 + (entries * 16 + 255) / 256 * 256;
+  }
+  plan->ml_bytes = 0;
+  plan->workspace = plan->list_bytes;
   if (plan->max_parts > 1) {
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan->max_parts;
-    const size_t ml = (rows * 2 * sizeof(float) + 255) / 256 * 256;
-    plan->workspace = ml + rows * c->head_dim * sizeof(float);
+    plan->ml_bytes = (rows * 2 * sizeof(float) + 255) / 256 * 256;
+    plan->workspace += plan->ml_bytes + rows * c->head_dim * sizeof(float);
   }
   return PKV_OK;
 }
@@ -258,11 +274,14 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.out = out;
-  if (plan.workspace > 0) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.max_parts;
-    const size_t ml = (rows * 2 * sizeof(float) + 255) / 256 * 256;
-    p.ws_ml = static_cast<float*>(workspace);
-    p.ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml);
+  if (plan.list_bytes > 0) {
+    p.work_count = static_cast<int*>(workspace);
+    p.work_list = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);
+  }
+  if (plan.max_parts > 1) {
+    char* base = static_cast<char*>(workspace) + plan.list_bytes;
+    p.ws_ml = reinterpret_cast<float*>(base);
+    p.ws_o = reinterpret_cast<float*>(base + plan.ml_bytes);
   }
   p.err = flag;
   p.num_seqs = num_seqs;

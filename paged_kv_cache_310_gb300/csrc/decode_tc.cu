@@ -100,27 +100,56 @@ struct TcArgs {
   DecodeParams p;
 };
 
-// Work item i -> (partition, sequence, kv head); partitions outermost.
+// One work item = (sequence, KV head, partition) with at least one token, packed by
+// the work-list kernel as {s, g, t0, ntok | nparts << 16}.
 struct Item {
-  int s, g, part, t0, ntok, nchunks, nparts, L;
+  int s, g, part, t0, ntok, nchunks, nparts;
 };
 
-__device__ __forceinline__ Item decode_item(const DecodeParams& p, int i) {
+__device__ __forceinline__ Item unpack_item(int4 e, int part_tokens) {
   Item it;
-  const int per_part = p.num_seqs * p.num_kv_heads;
-  it.part = i / per_part;
-  const int r = i - it.part * per_part;
-  it.s = r / p.num_kv_heads;
-  it.g = r - it.s * p.num_kv_heads;
-  it.L = p.context_lens[it.s];
-  it.t0 = it.part * p.part_tokens;
-  const bool bad = it.L < 0 || it.L > p.max_parts * p.part_tokens;
-  it.ntok = bad ? 0 : min(p.part_tokens, it.L - it.t0);
-  if (it.ntok < 0) it.ntok = 0;
+  it.s = e.x;
+  it.g = e.y;
+  it.t0 = e.z;
+  it.ntok = e.w & 0xffff;
+  it.nparts = static_cast<int>(static_cast<unsigned>(e.w) >> 16);
+  it.part = it.t0 / part_tokens;
   it.nchunks = (it.ntok + kChunk - 1) / kChunk;
-  it.nparts = (it.L + p.part_tokens - 1) / p.part_tokens;
   return it;
 }
+
+// Walks this CTA's items: the list is sorted longest first and dealt out in snake
+// order (round k goes left to right when k is even, right to left when odd), which
+// balances the CTAs to within about one chunk.  The next entry is always loaded one
+// item ahead so its latency hides behind the current item.
+struct ItemCursor {
+  const int4* list;
+  int count, k, idx, idx_next;
+  int4 cur, nxt;
+
+  __device__ __forceinline__ int snake(int r) const {
+    return r * static_cast<int>(gridDim.x) +
+           ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                    : static_cast<int>(blockIdx.x));
+  }
+  __device__ __forceinline__ void init(const int4* l, int n) {
+    list = l;
+    count = n;
+    k = 0;
+    idx = snake(0);
+    cur = idx < count ? list[idx] : make_int4(0, 0, 0, 0);
+    idx_next = snake(1);
+    nxt = idx_next < count ? list[idx_next] : make_int4(0, 0, 0, 0);
+  }
+  __device__ __forceinline__ bool valid() const { return idx < count; }
+  __device__ __forceinline__ void advance() {
+    ++k;
+    idx = idx_next;
+    cur = nxt;
+    idx_next = snake(k + 1);
+    if (idx_next < count) nxt = list[idx_next];
+  }
+};
 
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -178,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // chunks the producer issued
   int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // chunks the MMA lane saw land
   const int G = p.group;
-  const int total_items = p.max_parts * p.num_seqs * p.num_kv_heads;
+  const int num_items = *p.work_count;  // written by the work-list kernel earlier on the stream
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -219,9 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row outside the pool
     int c = 0, j = 0;
     bool ok = true;
-    for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
-      const Item it = decode_item(p, i);
-      if (it.ntok <= 0) continue;
+    ItemCursor cur;
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+      const Item it = unpack_item(cur.cur, p.part_tokens);
       const int qb = j & 1;
       if (lane == 0) {
         ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err);
@@ -279,24 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const uint32_t ring = smem_addr(smem);
       const uint32_t qbase = smem_addr(smem + kOffQ);
       const uint32_t pbase = smem_addr(smem + kOffP);
-      // QK cursor: item index, chunk within it, items started, chunks in the item
-      int qi = blockIdx.x, qk = 0, qj = 0, qn = 0;
-      auto next_item = [&]() {
-        for (; qi < total_items; qi += gridDim.x) {
-          const Item it = decode_item(p, qi);
-          if (it.ntok > 0) {
-            qn = it.nchunks;
-            return;
-          }
-        }
-        qn = 0;
-      };
-      next_item();
+      // QK cursor: items walked, chunk within the item, chunks in the item
+      ItemCursor qcur;
+      qcur.init(p.work_list, num_items);
+      int qk = 0, qj = 0;
+      int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
       int qc = 0, pc = 0;  // next chunk to QK, next chunk to PV
       uint64_t idle_since = global_timer_ns();
-      while (qi < total_items || pc < qc) {
+      while (qcur.valid() || pc < qc) {
         bool progressed = false;
-        if (qi < total_items) {
+        if (qcur.valid()) {
           const int st = qc % kStages, sb = qc & 1, qb = qj & 1;
           if ((qk > 0 || mbar_try_wait(&bars.qfull[qb], (qj >> 1) & 1)) &&
               mbar_try_wait(&bars.full[st], (qc / kStages) & 1) &&
@@ -318,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               mma_commit(&bars.qempty[qb]);
               qk = 0;
               ++qj;
-              qi += gridDim.x;
-              next_item();
+              qcur.advance();
+              qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
             }
             progressed = true;
           }
@@ -408,19 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     };
 
     bool prev_ok = true;  // outcome of the last consume (warp-uniform)
-    for (int i = blockIdx.x; i < total_items && ok; i += gridDim.x) {
-      const Item it = decode_item(p, i);
-      if (it.part == 0 && (it.L < 0 || it.L > p.max_parts * p.part_tokens)) {
-        if (t == 0) set_error(p.err, kErrLength);
-        continue;
-      }
-      if (it.L == 0 && it.part == 0) {  // empty context: the neutral output, no MMA work
-        for (int h = 0; h < G; ++h)
-          store_out<T>(p.out, (static_cast<size_t>(it.s) * p.num_q_heads + it.g * G + h) * 128 + t, 0.f,
-                       p.out_f32);
-        continue;
-      }
-      if (it.ntok <= 0) continue;
+    ItemCursor cur;
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+      const Item it = unpack_item(cur.cur, p.part_tokens);
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
         m[h] = -INFINITY;
@@ -546,6 +557,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Work list for the persistent kernel: one entry per (sequence, KV head, partition)
+// holding at least one token, sorted by chunk count, longest first (a counting sort
+// over at most 32 chunk counts; order inside one count does not matter, every item
+// is computed the same way wherever it runs).  Sequences of length 0 get their
+// all-zero output here; lengths outside [0, max_parts * part_tokens] set the flag.
+constexpr int kListThreads = 1024;
+constexpr int kMaxChunkCounts = kTcMaxPartition / kChunk;
+
+template <typename T>
+__global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ int hist[kMaxChunkCounts + 1];
+  __shared__ int next[kMaxChunkCounts + 1];
+  const int full_chunks = p.part_tokens / kChunk;
+  const int H = p.num_kv_heads;
+  for (int i = threadIdx.x; i <= kMaxChunkCounts; i += kListThreads) hist[i] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
+    const int L = p.context_lens[s];
+    if (L < 0 || L > p.max_parts * p.part_tokens) {
+      set_error(p.err, kErrLength);
+      continue;
+    }
+    const int nfull = L / p.part_tokens, rem = L - nfull * p.part_tokens;
+    if (nfull) atomicAdd(&hist[full_chunks], nfull * H);
+    if (rem) atomicAdd(&hist[(rem + kChunk - 1) / kChunk], H);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int c = kMaxChunkCounts; c >= 1; --c) {
+      next[c] = run;
+      run += hist[c];
+    }
+    *p.work_count = run;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
+    const int L = p.context_lens[s];
+    if (L <= 0 || L > p.max_parts * p.part_tokens) continue;
+    const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
+    for (int part = 0; part < nparts; ++part) {
+      const int t0 = part * p.part_tokens;
+      const int ntok = min(p.part_tokens, L - t0);
+      const int pos = atomicAdd(&next[(ntok + kChunk - 1) / kChunk], H);
+      for (int g = 0; g < H; ++g) p.work_list[pos + g] = make_int4(s, g, t0, ntok | (nparts << 16));
+    }
+  }
+  // empty contexts: the neutral output
+  const int row = p.num_q_heads * 128;
+  for (int s = 0; s < p.num_seqs; ++s) {
+    if (p.context_lens[s] != 0) continue;
+    for (int i = threadIdx.x; i < row; i += kListThreads)
+      store_out<T>(p.out, static_cast<size_t>(s) * row + i, 0.f, p.out_f32);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -624,11 +691,16 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
       !make_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
       !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16))
     return cudaErrorInvalidValue;
-  const int items = p.max_parts * p.num_seqs * p.num_kv_heads;
+  const int items = p.max_parts * p.num_seqs * p.num_kv_heads;  // upper bound on the list
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = items < sms ? items : sms;
-  if (grid == 0) return cudaSuccess;
+  if (bf16)
+    work_list_kernel<__nv_bfloat16><<<1, kListThreads, 0, stream>>>(p);
+  else
+    work_list_kernel<__half><<<1, kListThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || grid == 0) return e;
   return bf16 ? launch_tc_g<__nv_bfloat16>(args, grid, stream) : launch_tc_g<__half>(args, grid, stream);
 }
 

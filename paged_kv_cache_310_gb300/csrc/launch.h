@@ -19,6 +19,8 @@ struct DecodeParams {
   float* ws_o;   // [S][Hq][max_parts][D] un-normalised partition outputs (fp32)
   float* ws_ml;  // [S][Hq][max_parts][2] partition (max, sum) in the log2 domain
   int* err;      // device error flag
+  int4* work_list;  // tensor-core path: items sorted longest first (work-list kernel)
+  int* work_count;  // number of entries in work_list
   int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
   int32_t block_size, num_blocks, head_dim;
   int32_t part_tokens, max_parts;
@@ -28,7 +30,9 @@ struct DecodeParams {
 
 // CUDA-core split-K decode (any supported dtype, head_dim 64/128, group <= 8).
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t stream);
-// Tensor-core (tcgen05) decode: f16/bf16, head_dim 128, group <= 16, persistent CTAs.
+// Tensor-core (tcgen05) decode: f16/bf16, head_dim 128, group <= 16, persistent CTAs
+// fed by a work list that a one-CTA kernel builds first.  Partitions <= 4096 tokens.
+constexpr int kTcMaxPartition = 4096;
 bool tc_supported(int dtype, int head_dim, int group, int block_size);
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Partition merge for sequences longer than one partition.
