@@ -157,6 +157,33 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   const pkv_decode_config* config, void* stream);
 
 /*
+ * paged_attention_decode_no_alloc -- paged_attention_decode for callers that must not
+ * allocate device memory (allocator or memory-pool callbacks, serving paths that may
+ * not fail with out-of-memory once running, runtimes that only pass pre-registered
+ * buffers).  The pages have no counterpart: this is a packaging of the same decode.
+ *
+ * Same arguments and result as paged_attention_decode, minus the workspace: the
+ * scratch comes from a fixed array of paged_attention_no_alloc_limit() bytes
+ * (32 MiB) that every GPU loading the library holds until the process exits.  The
+ * call allocates nothing.  Sizes whose workspace would exceed the array return
+ * PKV_ERR_WORKSPACE (pass a larger partition_tokens, or use paged_attention_decode).
+ * The first call on a device looks up the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU (other streams, other threads)
+ * race on it and must be serialised by the caller.  Nothing in the array needs to
+ * start at zero; each call writes what it reads.
+ */
+pkv_status paged_attention_decode_no_alloc(const void* q, const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                           const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t max_context_len, float scale,
+                                           void* out, int32_t out_dtype, const pkv_cache_desc* cache,
+                                           const pkv_decode_config* config, void* stream);
+
+/* Bytes of the built-in array paged_attention_decode_no_alloc uses. */
+size_t paged_attention_no_alloc_limit(void);
+
+/*
  * paged_kv_gather -- the block-table lookup alone (testing the indexing bit-exactly):
  * k_out[s][h][j][:] = k_cache[block_tables[s][j / bs]][h][j % bs][:] for j < n_s,
  * same for v.  Rows j >= context_lens[s] are not written.

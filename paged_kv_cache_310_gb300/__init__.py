@@ -24,7 +24,8 @@ import torch
 __all__ = [
     "PagedKVError", "CacheDesc", "DecodeConfig", "library", "library_path", "cache_desc",
     "paged_kv_append", "paged_block_copy", "paged_attention_decode",
-    "paged_attention_workspace_bytes", "paged_kv_gather", "device_error", "declared_functions",
+    "paged_attention_workspace_bytes", "paged_attention_decode_no_alloc", "paged_attention_no_alloc_limit",
+    "paged_kv_gather", "device_error", "declared_functions",
     "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
 ]
 
@@ -85,6 +86,9 @@ def library():
             "paged_attention_decode": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                        vp, sz, desc_p, cfg_p, vp],
             "paged_kv_gather": [vp, vp, vp, i32, vp, i32, i32, vp, vp, desc_p, vp],
+            "paged_attention_decode_no_alloc": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp,
+                                                i32, desc_p, cfg_p, vp],
+            "paged_attention_no_alloc_limit": [],
             "paged_kv_device_error": [vp],
             "paged_kv_last_error": [],
             "paged_kv_version": [],
@@ -94,6 +98,7 @@ def library():
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.paged_attention_workspace_bytes.restype = sz
+        lib.paged_attention_no_alloc_limit.restype = sz
         lib.paged_kv_last_error.restype = ctypes.c_char_p
         lib.paged_kv_version.restype = ctypes.c_char_p
         _lib = lib
@@ -222,6 +227,34 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
                                       float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
                                       ws_bytes, ctypes.byref(desc), ctypes.byref(cfg), _stream(q)))
     return out
+
+
+def paged_attention_decode_no_alloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, *,
+                                    max_context_len: int | None = None, path: int = PATH_AUTO,
+                                    partition_tokens: int = 0) -> torch.Tensor:
+    """paged_attention_decode without a workspace argument, for callers that cannot
+    allocate device memory: the scratch is the library's built-in array of
+    ``paged_attention_no_alloc_limit()`` bytes per GPU, shared by every call (calls
+    that overlap on the GPU race on it)."""
+    _need_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
+    if q.dim() != 3 or out.shape != q.shape or q.dtype != k_cache.dtype or block_tables.dtype != torch.int32 \
+            or context_lens.dtype != torch.int32:
+        raise PagedKVError(1, "shape/dtype mismatch between q, out, the caches and the tables")
+    S, Hq, _ = q.shape
+    if max_context_len is None:
+        max_context_len = int(context_lens.max()) if S else 0
+    desc = cache_desc(k_cache)
+    cfg = _config(path, partition_tokens)
+    _check(library().paged_attention_decode_no_alloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, Hq,
+        max_context_len, float(scale), _ptr(out), DTYPE_CODE[out.dtype], ctypes.byref(desc), ctypes.byref(cfg),
+        _stream(q)))
+    return out
+
+
+def paged_attention_no_alloc_limit() -> int:
+    """Bytes of the built-in workspace array used by paged_attention_decode_no_alloc."""
+    return int(library().paged_attention_no_alloc_limit())
 
 
 def paged_kv_gather(k_cache, v_cache, block_tables, context_lens, k_out, v_out, *,

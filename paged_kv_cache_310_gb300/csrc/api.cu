@@ -140,6 +140,9 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
 }
 
 }  // namespace
+
+pkv_status record_error(pkv_status status, const char* message) { return fail(status, "%s", message); }
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pagedkv.h"
+
 namespace pkv {
 
 // Everything decode kernels need, by value (one __grid_constant__ struct).
@@ -37,6 +39,9 @@ bool tc_supported(int dtype, int head_dim, int group, int block_size);
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Partition merge for sequences longer than one partition.
 cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
+
+// Records a failure message for paged_kv_last_error() on this host thread.
+pkv_status record_error(pkv_status status, const char* message);
 
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t num_tokens,
                           void* k_cache, void* v_cache, int32_t num_kv_heads, int32_t block_size,
