@@ -231,10 +231,8 @@ def main():
     if pkv.device_error() != 0:
         raise SystemExit("device error flag set during warm-up")
 
-    launches_per_step = (1 if g.cow_pairs.numel() else 0) + 1 + 1
-    ws_parts = pkv.paged_attention_workspace_bytes(S, Hq, maxL, g.k_cache, path=path,
-                                                   partition_tokens=args.partition) > 0
-    launches_per_step += 1 if ws_parts else 0
+    plan = pkv.paged_attention_plan(S, Hq, maxL, g.k_cache, path=path, partition_tokens=args.partition)
+    launches_per_step = (1 if g.cow_pairs.numel() else 0) + 1 + plan["kernel_launches"]
 
     # ---------------- device-timed region ----------------
     clocks = ClockSampler(local)
@@ -306,7 +304,8 @@ def main():
         "vs_baseline": None, "dtype": workloads.DTYPE_NAMES[w.dtype], "data": "synthetic",
         "config": {"workload": w.name, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": w.num_kv_heads,
                    "head_dim": D, "block_size": w.block_size, "sum_context_tokens": tokens,
-                   "kv_bytes_per_step": kv_bytes, "path": args.path, "partition_tokens": args.partition,
+                   "kv_bytes_per_step": kv_bytes, "path": {1: "cuda_core", 2: "tensor_core"}[plan["path"]],
+                   "partition_tokens": plan["partition_tokens"], "partitions": plan["max_partitions"],
                    "l2": f"inputs larger than L2 (KV {kv_bytes / 1e9:.2f} GB > 129 MB): no flush",
                    "parallelism": f"replicas x{world}"},
         "seq_tokens_per_s": world * tokens / (ms_per_step * 1e-3),

@@ -119,6 +119,26 @@ pkv_status paged_block_copy(const int64_t* src_dst_pairs, const int64_t* host_pa
                             int32_t num_pairs, void* k_cache, void* v_cache,
                             const pkv_cache_desc* cache, void* stream);
 
+/* What paged_attention_decode will do for these sizes and config. */
+typedef struct {
+  int32_t path;              /* pkv_path actually taken (never PKV_PATH_AUTO) */
+  int32_t partition_tokens;  /* tokens per split-K partition */
+  int32_t max_partitions;    /* partitions of the longest sequence (1 = no merge) */
+  int32_t kernel_launches;   /* kernels one call enqueues */
+  size_t workspace_bytes;    /* as paged_attention_workspace_bytes */
+} pkv_decode_plan;
+
+/*
+ * paged_attention_plan -- fill *out with the plan paged_attention_decode follows for
+ * these arguments (host only, no device work).  Automatic partitions: 512 tokens on
+ * CUDA cores; on tensor cores the largest size up to 4096 that leaves about four
+ * (sequence, KV head, partition) items per SM.  Errors as paged_attention_decode's
+ * argument checks.
+ */
+pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                const pkv_cache_desc* cache, const pkv_decode_config* config,
+                                pkv_decode_plan* out);
+
 /*
  * Bytes of workspace paged_attention_decode needs for these sizes and config.  The
  * CUDA-core path needs none when every sequence fits one partition; the tensor-core

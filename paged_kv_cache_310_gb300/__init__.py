@@ -22,7 +22,7 @@ import threading
 import torch
 
 __all__ = [
-    "PagedKVError", "CacheDesc", "DecodeConfig", "library", "library_path", "cache_desc",
+    "PagedKVError", "CacheDesc", "DecodeConfig", "DecodePlan", "paged_attention_plan", "library", "library_path", "cache_desc",
     "paged_kv_append", "paged_block_copy", "paged_attention_decode",
     "paged_attention_workspace_bytes", "paged_attention_decode_no_alloc", "paged_attention_no_alloc_limit",
     "paged_kv_gather", "device_error", "declared_functions",
@@ -57,6 +57,12 @@ class DecodeConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("partition_tokens", ctypes.c_int32)]
 
 
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("partition_tokens", ctypes.c_int32),
+                ("max_partitions", ctypes.c_int32), ("kernel_launches", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -83,6 +89,7 @@ def library():
             "paged_kv_append": [vp, vp, vp, i32, vp, vp, desc_p, vp],
             "paged_block_copy": [vp, vp, i32, vp, vp, desc_p, vp],
             "paged_attention_workspace_bytes": [i32, i32, i32, desc_p, cfg_p],
+            "paged_attention_plan": [i32, i32, i32, desc_p, cfg_p, ctypes.POINTER(DecodePlan)],
             "paged_attention_decode": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                        vp, sz, desc_p, cfg_p, vp],
             "paged_kv_gather": [vp, vp, vp, i32, vp, i32, i32, vp, vp, desc_p, vp],
@@ -175,6 +182,18 @@ def paged_attention_workspace_bytes(num_seqs, num_q_heads, max_context_len, k_ca
     cfg = _config(path, partition_tokens)
     return int(library().paged_attention_workspace_bytes(num_seqs, num_q_heads, max_context_len,
                                                          ctypes.byref(desc), ctypes.byref(cfg)))
+
+
+def paged_attention_plan(num_seqs, num_q_heads, max_context_len, k_cache, *, path=PATH_AUTO,
+                         partition_tokens=0) -> dict:
+    """The path, partition size, partition count, kernel launches and workspace bytes
+    paged_attention_decode uses for these sizes."""
+    desc = cache_desc(k_cache)
+    cfg = _config(path, partition_tokens)
+    plan = DecodePlan()
+    _check(library().paged_attention_plan(num_seqs, num_q_heads, max_context_len, ctypes.byref(desc),
+                                          ctypes.byref(cfg), ctypes.byref(plan)))
+    return {f: getattr(plan, f) for f, _ in DecodePlan._fields_}
 
 
 _ws_cache: dict = {}

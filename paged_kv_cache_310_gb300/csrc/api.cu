@@ -113,7 +113,16 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
     return fail(PKV_ERR_INVALID_ARG, "tensor-core partitions are at most %d tokens (%d asked)",
                 kTcMaxPartition, part);
   if (part == 0) {
-    const int auto_part = path == PKV_PATH_TENSOR_CORE ? 1024 : 512;
+    int auto_part = 512;
+    if (path == PKV_PATH_TENSOR_CORE) {
+      // Persistent CTAs balance well with >= ~4 items per SM (GB300: 152 SMs): take
+      // the largest partition (fewest items, no merge when a sequence fits) that
+      // still leaves about that many, assuming lengths average half the maximum.
+      const int64_t work = static_cast<int64_t>(num_seqs) * c->num_kv_heads * (max_len / 2 + 1);
+      const int64_t per_item = work / (4 * 152) + 1;
+      auto_part = static_cast<int>(per_item > kTcMaxPartition ? kTcMaxPartition : per_item);
+      auto_part = round_up(auto_part < 512 ? 512 : auto_part, 128);
+    }
     part = max_len <= auto_part ? (max_len < 128 ? 128 : round_up(max_len, 128)) : auto_part;
   }
   plan->path = path;
@@ -227,6 +236,21 @@ pkv_status paged_block_copy(const int64_t* src_dst_pairs, const int64_t* host_pa
   cudaError_t e = launch_block_copy(src_dst_pairs, num_pairs, k_cache, v_cache, block_bytes,
                                     cache->num_blocks, flag, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "block copy launch");
+}
+
+pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                const pkv_cache_desc* cache, const pkv_decode_config* config,
+                                pkv_decode_plan* out) {
+  if (!out) return fail(PKV_ERR_INVALID_ARG, "plan output is NULL");
+  DecodePlan plan;
+  if (pkv_status st = plan_decode(num_seqs, num_q_heads, max_context_len, cache, config, &plan)) return st;
+  out->path = plan.path;
+  out->partition_tokens = plan.part_tokens;
+  out->max_partitions = plan.max_parts;
+  out->kernel_launches = num_seqs == 0 ? 0
+                         : 1 + (plan.path == PKV_PATH_TENSOR_CORE ? 1 : 0) + (plan.max_parts > 1 ? 1 : 0);
+  out->workspace_bytes = plan.workspace;
+  return PKV_OK;
 }
 
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,

@@ -125,3 +125,16 @@ def test_binding_fails_loudly_without_a_gpu():
     k = torch.zeros(2, 1, 16, 64)
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_kv_append(k[:, 0, :1], k[:, 0, :1], torch.zeros(2, dtype=torch.int64), k, k)
+
+
+def test_plan_reports_path_partitions_and_launches(lib):
+    k16 = __import__("torch").empty((1, 8, 16, 128), dtype=__import__("torch").bfloat16)
+    p = pkv.paged_attention_plan(128, 64, 4096, k16)            # GQA group 8 -> tensor cores
+    assert p["path"] == pkv.PATH_TENSOR_CORE and p["partition_tokens"] % 128 == 0
+    assert p["partition_tokens"] <= 4096 and p["kernel_launches"] == 2 + (p["max_partitions"] > 1)
+    p1 = pkv.paged_attention_plan(64, 8, 2048, k16)             # group 1 -> CUDA cores, 512-token partitions
+    assert p1["path"] == pkv.PATH_CUDA_CORE and p1["partition_tokens"] == 512 and p1["max_partitions"] == 4
+    assert p1["kernel_launches"] == 2
+    assert pkv.paged_attention_plan(64, 8, 300, k16)["kernel_launches"] == 1   # one partition, no merge
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_attention_plan(64, 8, 2048, k16, path=pkv.PATH_TENSOR_CORE, partition_tokens=8192)
