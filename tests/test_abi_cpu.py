@@ -54,7 +54,7 @@ def test_workspace_sizes(lib):
     # the tensor-core path (chosen automatically for groups >= 2) splits at 1024 tokens
     assert _ws(lib, 64, 32, 2048, d) == _ws(lib, 64, 32, 2048, d, path=tensor)
     # one partition: the tensor-core path still needs its work list (16 B per item + header)
-    assert _ws(lib, 64, 32, 1024, d, path=tensor) == 256 + -(-64 * 8 * 16 // 256) * 256
+    assert _ws(lib, 64, 32, 1024, d, path=tensor, part=1024) == 256 + -(-64 * 8 * 16 // 256) * 256
     assert _ws(lib, 64, 32, 2048, d, path=tensor, part=8192) == 0  # partitions <= 4096 on tensor cores
     assert _ws(lib, 64, 32, 2048, d, part=100) == 0       # invalid partition size
     assert _ws(lib, 64, 30, 2048, d) == 0                 # heads not a multiple of kv heads
