@@ -131,7 +131,7 @@ typedef struct {
 /*
  * paged_attention_plan -- fill *out with the plan paged_attention_decode follows for
  * these arguments (host only, no device work).  Automatic partitions: 512 tokens on
- * CUDA cores; on tensor cores the largest size up to 4096 that leaves about four
+ * CUDA cores; on tensor cores the largest size up to 4096 that leaves about three
  * (sequence, KV head, partition) items per SM.  Errors as paged_attention_decode's
  * argument checks.
  */

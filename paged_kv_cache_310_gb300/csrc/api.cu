@@ -115,11 +115,11 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   if (part == 0) {
     int auto_part = 512;
     if (path == PKV_PATH_TENSOR_CORE) {
-      // Persistent CTAs balance well with >= ~4 items per SM (GB300: 152 SMs): take
+      // Persistent CTAs balance well with >= ~3 items per SM (GB300: 152 SMs): take
       // the largest partition (fewest items, no merge when a sequence fits) that
       // still leaves about that many, assuming lengths average half the maximum.
       const int64_t work = static_cast<int64_t>(num_seqs) * c->num_kv_heads * (max_len / 2 + 1);
-      const int64_t per_item = work / (4 * 152) + 1;
+      const int64_t per_item = work / (3 * 152) + 1;
       auto_part = static_cast<int>(per_item > kTcMaxPartition ? kTcMaxPartition : per_item);
       auto_part = round_up(auto_part < 512 ? 512 : auto_part, 128);
     }
