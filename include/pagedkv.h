@@ -130,10 +130,11 @@ typedef struct {
 
 /*
  * paged_attention_plan -- fill *out with the plan paged_attention_decode follows for
- * these arguments (host only, no device work).  Automatic partitions: 512 tokens on
- * CUDA cores; on tensor cores the largest size up to 4096 that leaves about three
- * (sequence, KV head, partition) items per SM.  Errors as paged_attention_decode's
- * argument checks.
+ * these arguments (host only, no device work).  Automatic partitions: on CUDA cores
+ * 512 to 2048 tokens, aiming at about 12 CTAs per SM; on tensor cores the largest
+ * size up to 4096 that leaves about three (sequence, KV head, partition) items per SM
+ * (lengths assumed to average half of max_context_len).  Errors as
+ * paged_attention_decode's argument checks.
  */
 pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
                                 const pkv_cache_desc* cache, const pkv_decode_config* config,

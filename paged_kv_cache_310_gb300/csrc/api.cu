@@ -114,7 +114,14 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
                 kTcMaxPartition, part);
   if (part == 0) {
     int auto_part = 512;
-    if (path == PKV_PATH_TENSOR_CORE) {
+    if (path == PKV_PATH_CUDA_CORE) {
+      // one CTA per (partition, KV head, sequence): aim for about 12 CTAs per SM
+      // (several waves of three resident CTAs), partitions of 512 to 2048 tokens
+      const int64_t work = static_cast<int64_t>(num_seqs) * c->num_kv_heads * (max_len / 2 + 1);
+      const int64_t per_cta = work / (12 * 152) + 1;
+      auto_part = static_cast<int>(per_cta > 2048 ? 2048 : per_cta);
+      auto_part = round_up(auto_part < 512 ? 512 : auto_part, 128);
+    } else {
       // Persistent CTAs balance well with >= ~3 items per SM (GB300: 152 SMs): take
       // the largest partition (fewest items, no merge when a sequence fits) that
       // still leaves about that many, assuming lengths average half the maximum.

@@ -604,12 +604,12 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
       for (int g = 0; g < H; ++g) p.work_list[pos + g] = make_int4(s, g, t0, ntok | (nparts << 16));
     }
   }
-  // empty contexts: the neutral output
+  // empty contexts: the neutral output, one warp per sequence
   const int row = p.num_q_heads * 128;
-  for (int s = 0; s < p.num_seqs; ++s) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int s = warp; s < p.num_seqs; s += kListThreads / 32) {
     if (p.context_lens[s] != 0) continue;
-    for (int i = threadIdx.x; i < row; i += kListThreads)
-      store_out<T>(p.out, static_cast<size_t>(s) * row + i, 0.f, p.out_f32);
+    for (int i = lane; i < row; i += 32) store_out<T>(p.out, static_cast<size_t>(s) * row + i, 0.f, p.out_f32);
   }
 }
 
