@@ -71,7 +71,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # PKV_ORACLE_LIB points the pins at another build of this file (the
+            # mutation tests use it to show that planted mistakes are caught)
+            lib = ctypes.CDLL(os.environ.get("PKV_ORACLE_LIB") or build())
             i32, i64, dbl, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
             lib.pkvo_decode.argtypes = [i32, vp, i64, vp]
             lib.pkvo_max_threads.restype = i32
