@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size (8/16/32)")
+    ap.add_argument("--identity-tables", action="store_true",
+                    help="physical blocks in logical order (contiguous sequences): the indirection A/B")
     return ap.parse_args()
 
 
@@ -204,7 +207,9 @@ def main():
 
     path = {"auto": pkv.PATH_AUTO, "cuda_core": pkv.PATH_CUDA_CORE, "tensor_core": pkv.PATH_TENSOR_CORE}[args.path]
     # every rank decodes its own batch of the same workload shape (independent replicas)
-    w = workloads.make_workload(args.config, canary=False, pool_device=dev)
+    overrides = {"block_size": args.block_size} if args.block_size else {}
+    w = workloads.make_workload(args.config, canary=False, pool_device=dev, shuffle=not args.identity_tables,
+                                **overrides)
     g = w.to(dev)
     S, Hq, D = g.q.shape
     out = torch.empty((S, Hq, D), dtype=w.dtype, device=dev)
@@ -307,7 +312,8 @@ def main():
                    "kv_bytes_per_step": kv_bytes, "path": {1: "cuda_core", 2: "tensor_core"}[plan["path"]],
                    "partition_tokens": plan["partition_tokens"], "partitions": plan["max_partitions"],
                    "l2": f"inputs larger than L2 (KV {kv_bytes / 1e9:.2f} GB > 129 MB): no flush",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "block_tables": "identity" if args.identity_tables
+                   else "shuffled"},
         "seq_tokens_per_s": world * tokens / (ms_per_step * 1e-3),
         "hbm_frac_step": (algo_bytes / (ms_per_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -225,6 +225,16 @@ const char* paged_kv_last_error(void);
  */
 pkv_status paged_kv_device_error(void* stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): enqueue one kernel whose bounded wait can
+ * never complete -- an mbarrier expecting an arrival nobody makes -- so that the wait
+ * gives up after limit_ns (at most 5 s), records PKV_ERR_DEVICE_TIMEOUT in the device
+ * flag and returns.  Shows that a stuck wait ends with a status the host reads and
+ * leaves the context usable; every wait in the library's kernels ends the same way
+ * (their limit is 2 s).
+ */
+pkv_status paged_kv_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
 /* Library version, e.g. "0.1.0". */
 const char* paged_kv_version(void);
 

@@ -97,6 +97,7 @@ def library():
                                                 i32, desc_p, cfg_p, vp],
             "paged_attention_no_alloc_limit": [],
             "paged_kv_device_error": [vp],
+            "paged_kv_selftest_wait_timeout": [ctypes.c_uint64, vp],
             "paged_kv_last_error": [],
             "paged_kv_version": [],
         }
@@ -290,6 +291,12 @@ def paged_kv_gather(k_cache, v_cache, block_tables, context_lens, k_out, v_out, 
     _check(library().paged_kv_gather(_ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
                                      _ptr(context_lens), S, max_context_len, _ptr(k_out), _ptr(v_out),
                                      ctypes.byref(desc), _stream(k_cache)))
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000) -> None:
+    """Run the bounded-wait self-test kernel on the current stream (see the header)."""
+    stream = torch.cuda.current_stream()
+    _check(library().paged_kv_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(stream.cuda_stream)))
 
 
 def device_error(device=None) -> int:

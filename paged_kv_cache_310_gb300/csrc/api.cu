@@ -188,6 +188,15 @@ pkv_status paged_kv_device_error(void* stream) {
   return PKV_OK;
 }
 
+pkv_status paged_kv_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 5000000000ull)
+    return fail(PKV_ERR_INVALID_ARG, "limit_ns %llu outside (0, 5 s]", (unsigned long long)limit_ns);
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  cudaError_t e = launch_wait_timeout_selftest(limit_ns, flag, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "self-test launch");
+}
+
 pkv_status paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping,
                            int32_t num_tokens, void* k_cache, void* v_cache,
                            const pkv_cache_desc* cache, void* stream) {

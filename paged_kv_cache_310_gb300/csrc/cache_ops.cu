@@ -107,7 +107,24 @@ gather_kernel(const uint4* __restrict__ kc, const uint4* __restrict__ vc,
   }
 }
 
+// Self-test of the bounded wait: an mbarrier that expects one arrival nobody makes.
+// The wait gives up after limit_ns, sets the timeout flag and the kernel returns.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) set_error(err, kErrTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t num_tokens,
                           void* k_cache, void* v_cache, int32_t num_kv_heads, int32_t block_size,

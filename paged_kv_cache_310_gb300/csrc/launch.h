@@ -43,6 +43,9 @@ cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Records a failure message for paged_kv_last_error() on this host thread.
 pkv_status record_error(pkv_status status, const char* message);
 
+// Diagnostic: one bounded wait that cannot complete (see paged_kv_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream);
+
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slots, int32_t num_tokens,
                           void* k_cache, void* v_cache, int32_t num_kv_heads, int32_t block_size,
                           int32_t row_bytes, int64_t num_slots, int* err, cudaStream_t stream);

@@ -266,3 +266,18 @@ def test_binding_rejects_bad_arguments():
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_block_copy(torch.tensor([[1, 1]], device="cuda"), g.k_cache, g.v_cache,
                              host_pairs=torch.tensor([[1, 1]]))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that cannot complete gives up, sets the timeout status, and the GPU keeps working."""
+    import time
+    t0 = time.perf_counter()
+    pkv.selftest_wait_timeout(50_000_000)  # 50 ms
+    assert pkv.device_error() == 6        # PKV_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    assert pkv.device_error() == 0        # read-and-clear
+    w = workloads.random_workload(11, num_seqs=3, max_len=300, min_len=1, num_q_heads=8, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="bf16")
+    ref, kc, vc = oracle_step(w)
+    out, _ = gpu_step(w, torch.float32)
+    check_close(out, ref, w.dtype)

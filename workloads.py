@@ -104,7 +104,7 @@ def _randn(shape, gen, dtype, device="cpu"):
 
 def build_from_layout(*, name, seed, dtype, num_q_heads, num_kv_heads, head_dim, block_size,
                       ctx, block_keys, owned_rows, cow, num_blocks=None, canary=True,
-                      pool_device="cpu", gen=None, meta=None) -> Workload:
+                      pool_device="cpu", gen=None, meta=None, shuffle=True) -> Workload:
     """Materialise a workload from a logical layout.
 
     ctx[s]          -- tokens sequence s attends over (its append writes position ctx[s]-1).
@@ -129,7 +129,9 @@ def build_from_layout(*, name, seed, dtype, num_q_heads, num_kv_heads, head_dim,
     if num_blocks is None:
         num_blocks = max(1, math.ceil(1.25 * unique))
     assert num_blocks >= unique
-    perm = torch.randperm(num_blocks, generator=g)
+    # shuffle=False lays blocks out in logical order: each sequence contiguous, the
+    # identity-table arrangement used to measure what the indirection costs
+    perm = torch.randperm(num_blocks, generator=g) if shuffle else torch.arange(num_blocks)
     phys = {k: int(perm[i]) for i, k in enumerate(order)}
 
     max_blocks = max((len(k) for k in block_keys), default=1)
@@ -189,8 +191,13 @@ def private_layout(ctx, block_size):
     return keys, owned
 
 
-def make_workload(config: int, *, canary: bool = True, pool_device="cpu", **overrides) -> Workload:
-    """One of the five numbered workloads (seed 310000 + config)."""
+def make_workload(config: int, *, canary: bool = True, pool_device="cpu", shuffle: bool = True,
+                  **overrides) -> Workload:
+    """One of the five numbered workloads (seed 310000 + config).
+
+    overrides replace fields of the workload (e.g. block_size); shuffle=False assigns
+    physical blocks in logical order instead of by a seeded permutation.
+    """
     c = dict(CONFIGS[config])
     c.update(overrides)
     seed = SEED_BASE + config
@@ -198,7 +205,7 @@ def make_workload(config: int, *, canary: bool = True, pool_device="cpu", **over
     bs = c["block_size"]
     common = dict(name=c["name"], seed=seed, dtype=c["dtype"], num_q_heads=c["num_q_heads"],
                   num_kv_heads=c["num_kv_heads"], head_dim=c["head_dim"], block_size=bs,
-                  canary=canary, pool_device=pool_device, gen=g)
+                  canary=canary, pool_device=pool_device, gen=g, shuffle=shuffle)
     kind = c["kind"]
     if kind == "tiny":
         before = [1, 15, 16, 33]
