@@ -18,8 +18,8 @@
 // Persistent CTAs (one per SM, static round-robin over work items = (partition,
 // sequence, KV head)), 192 threads in four roles:
 //  * warp 4, producer: per 128-token chunk, one lane per physical block reads the
-//    block id (before waiting for a free stage, hiding its latency) and issues four
-//    tiled TMA loads (K and V, two 64-column halves each,
+//    block id (before waiting for a free stage, hiding its latency) and issues two
+//    tiled TMA loads (the block's K tile and V tile for this KV head, 4-D boxes,
 //    128-byte swizzle) into a 3-stage ring; blocks past the item's end are loaded
 //    from outside the tensor, which the TMA unit fills with zeros.  It also loads the
 //    item's 16 query rows.
@@ -50,8 +50,14 @@ constexpr int kThreads = 192;
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
 constexpr int kStages = 3;
 constexpr int kN = 16;                         // MMA N: query heads per group, padded
-constexpr int kHalf = kChunk * 128;            // one 64-column half of a K or V tile: 16 KB
-constexpr int kStageBytes = 4 * kHalf;         // K lo, K hi, V lo, V hi
+// A chunk's K (and V) sits in shared memory as [8-row group][64-column half][8 rows]
+// of 128-byte rows: 16 groups x 2 halves x 1 KB = 32 KB, 128-byte swizzled.  That is
+// the canonical K-major layout for the QK A operand (8-row groups 2 KB apart, halves
+// 1 KB apart) and the MN-major layout for the PV A operand V^T (8-token groups 2 KB
+// apart, 64-dimension blocks 1 KB apart), and one 4-D TMA box fills a whole block.
+constexpr int kGroupBytes = 2048;               // one 8-row group: both halves
+constexpr int kTileBytes = kChunk * 256;        // K or V of one chunk: 32 KB
+constexpr int kStageBytes = 2 * kTileBytes;     // K then V
 constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 128 B
 constexpr int kPBytes = 2 * kChunk * 16;       // 4 KB: two groups of 8 heads
 constexpr int kOffQ = kStages * kStageBytes;
@@ -94,7 +100,7 @@ __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
 }
 
 struct TcArgs {
-  CUtensorMap tk;  // K pool as [NB*Hkv*bs rows, 128], box 64 x bs, 128-byte swizzle
+  CUtensorMap tk;  // K pool, 4-D view (see make_pool_map): one box = one block's tile
   CUtensorMap tv;  // V pool, same
   CUtensorMap tq;  // q as [S*Hq rows, 128], box 64 x 16
   DecodeParams p;
@@ -286,11 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             row = (b * p.num_kv_heads + it.g) * bs;
           }
-          unsigned char* dst = smem + st * kStageBytes + lane * bs * 128;
-          tma_load_2d(dst, &a.tk, 0, row, &bars.full[st], pol_stream);
-          tma_load_2d(dst + kHalf, &a.tk, 64, row, &bars.full[st], pol_stream);
-          tma_load_2d(dst + 2 * kHalf, &a.tv, 0, row, &bars.full[st], pol_stream);
-          tma_load_2d(dst + 3 * kHalf, &a.tv, 64, row, &bars.full[st], pol_stream);
+          unsigned char* dst = smem + st * kStageBytes + lane * bs * 256;
+          tma_load_4d(dst, &a.tk, row / 8, &bars.full[st], pol_stream);
+          tma_load_4d(dst + kTileBytes, &a.tv, row / 8, &bars.full[st], pol_stream);
         }
         if (lane == 0) *issued_slot = c + 1;
       }
@@ -328,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             const uint32_t qa = qbase + qb * kQBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kLayoutSwizzle128);
+              const uint64_t ad = smem_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kGroupBytes,
+                                            kLayoutSwizzle128);
               const uint64_t bd = smem_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024,
                                             kLayoutSwizzle128);
               mma_f16(tmem + sb * 16, ad, bd, idesc_qk, kk > 0);
@@ -350,10 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           if (mbar_try_wait(&bars.pfull[pb], (pc >> 1) & 1) &&
               (pc < 2 || mbar_try_wait(&bars.ofree[pb], ((pc >> 1) - 1) & 1))) {
             tc_fence_after();
-            const uint32_t vbase = ring + st * kStageBytes + 2 * kHalf;
+            const uint32_t vbase = ring + st * kStageBytes + kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < kChunk / 16; ++kk) {
-              const uint64_t ad = smem_desc(vbase + kk * 2048, kHalf, 1024, kLayoutSwizzle128);
+              const uint64_t ad = smem_desc(vbase + kk * 2 * kGroupBytes, 1024, kGroupBytes, kLayoutSwizzle128);
               const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
               mma_f16(tmem + 32 + pb * 16, ad, bd, idesc_pv, kk > 0);
             }
@@ -487,11 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // rows of the last loaded block past the context end: zero their V rows
         const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
         if (t >= rows_valid && t < rows_loaded) {
-          unsigned char* vrow = smem + (c % kStages) * kStageBytes + 2 * kHalf + t * 128;
+          unsigned char* vrow = smem + (c % kStages) * kStageBytes + kTileBytes + (t >> 3) * kGroupBytes +
+                                (t & 7) * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(vrow + kHalf)[q] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(vrow + 1024)[q] = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
@@ -631,6 +637,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Pool of rows of 128 16-bit elements seen as 4-D: (64 columns, 8 rows, 2 halves,
+// 8-row groups) with byte strides (-, 256, 128, 2048).  A box of (64, 8, 2, bs/8)
+// is one block's tile for one KV head, landing as [group][half][row][64 columns].
+bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows % 8) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, block_size / 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over rows of 128 16-bit elements, box 64 x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16) {
   EncodeTiledFn fn = encode_fn();
@@ -687,8 +709,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
-      !make_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
+  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
+      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
       !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16))
     return cudaErrorInvalidValue;
   const int items = p.max_parts * p.num_seqs * p.num_kv_heads;  // upper bound on the list
