@@ -67,7 +67,8 @@ typedef enum {
   PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
   PKV_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
   PKV_ERR_DEVICE_INDEX = 5,   /* a kernel met an out-of-range block id, slot or length */
-  PKV_ERR_DEVICE_TIMEOUT = 6  /* a kernel's bounded wait ran out (copy never landed) */
+  PKV_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out (copy never landed) */
+  PKV_ERR_OUT_OF_BLOCKS = 7   /* block manager: not enough free physical blocks */
 } pkv_status;
 
 /* Geometry of one layer's block pool (both k_cache and v_cache). */
@@ -214,6 +215,60 @@ pkv_status paged_kv_gather(const void* k_cache, const void* v_cache, const int32
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
                            int32_t num_seqs, int32_t max_context_len, void* k_out, void* v_out,
                            const pkv_cache_desc* cache, void* stream);
+
+/* ----------------------------------------------------------------------------------
+ * Host block manager: which physical block every token lives in.
+ * Pages: note-023, Method (allocate on demand as a sequence grows, free when it
+ * finishes, share blocks between sequences with identical prefixes, copy on write when
+ * one diverges) and Concepts (internal fragmentation = unused tail of the last block);
+ * "Paged Attention" glossary, paragraphs 1-3; "PagedAttention & Continuous Batching",
+ * shared-system-prompt paragraph (blocks of a finished request go to the next one).
+ *
+ * Host memory only; not thread-safe (one manager per host thread, or a caller lock).
+ * Policy: free blocks form a LIFO stack (first hands out 0, 1, 2, ...; freed blocks are
+ * reused first).  Every call either succeeds as a whole or changes nothing.
+ * ---------------------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+typedef struct {
+  int32_t num_blocks, free_blocks, used_blocks, num_sequences;
+  int32_t shared_blocks;   /* blocks referenced by more than one sequence */
+  int64_t stored_tokens;   /* valid rows held in used blocks (shared rows counted once) */
+  int64_t logical_tokens;  /* sum of sequence lengths (shared rows counted per sharer) */
+  int64_t allocated_slots; /* used_blocks * block_size */
+  int64_t max_len;         /* longest sequence */
+  int64_t copies;          /* copy-on-write copies made so far */
+} pkv_block_stats;
+
+/* A manager for a pool of num_blocks blocks of block_size tokens.  Free with destroy. */
+pkv_status pkv_bm_create(int32_t num_blocks, int32_t block_size, pkv_block_manager** out);
+void pkv_bm_destroy(pkv_block_manager* manager);
+
+/* A new sequence with a prompt of num_tokens tokens: ceil(num_tokens / block_size)
+ * fresh blocks.  PKV_ERR_OUT_OF_BLOCKS if the pool cannot hold them. */
+pkv_status pkv_bm_add_sequence(pkv_block_manager* manager, int64_t seq_id, int64_t num_tokens);
+
+/* child shares every block of parent by reference (parallel sampling, beam search). */
+pkv_status pkv_bm_fork(pkv_block_manager* manager, int64_t parent, int64_t child);
+
+/*
+ * Reserve the slot of one new token for each of n distinct sequences, in order.  A
+ * sequence at a block boundary takes a fresh block; one whose last block is shared
+ * gets a fresh copy of it first (copy-on-write) and the pair (old, fresh) is appended
+ * to cow_pairs ([n][2] capacity, *num_cow set).  slots[i] = block * block_size + row,
+ * ready for paged_kv_append; apply the pairs with paged_block_copy before the append.
+ */
+pkv_status pkv_bm_append(pkv_block_manager* manager, const int64_t* seq_ids, int32_t n, int64_t* slots,
+                         int64_t* cow_pairs, int32_t* num_cow);
+
+/* The sequence finished: drop its references; blocks no longer referenced are freed. */
+pkv_status pkv_bm_free_sequence(pkv_block_manager* manager, int64_t seq_id);
+
+/* Rows of block_tables ([n][max_blocks], -1 padded) and context_lens for n sequences. */
+pkv_status pkv_bm_block_tables(const pkv_block_manager* manager, const int64_t* seq_ids, int32_t n,
+                               int32_t max_blocks, int32_t* tables, int32_t* lens);
+
+pkv_status pkv_bm_stats(const pkv_block_manager* manager, pkv_block_stats* out);
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* paged_kv_last_error(void);
