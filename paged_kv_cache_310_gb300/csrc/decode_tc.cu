@@ -29,10 +29,10 @@
 //    the softmax warps.
 //  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
 //    chunk max across the 128 tokens (shuffles + shared memory), online-softmax
-//    rescale, probabilities rounded to the cache dtype into P^T (shared memory), then
-//    read O row t (dimension t) of the previous chunk and accumulate it in registers
-//    with the rescale factor.  The row sum uses the rounded probabilities, so the
-//    output is an exact convex combination of the V rows with those weights.
+//    rescale, probabilities split into two parts rounded to the cache dtype
+//    (hi = round(p), lo = round(p - hi)) into P^T (shared memory), then read O row t
+//    (dimension t) of the previous chunk, add its hi and lo columns and accumulate in
+//    registers with the rescale factor.
 //  Rows of the last block past the context end hold real cache data; the softmax
 //  warps zero those V rows in shared memory before PV (a NaN there would survive a
 //  zero weight).
@@ -59,7 +59,12 @@ constexpr int kGroupBytes = 2048;               // one 8-row group: both halves
 constexpr int kTileBytes = kChunk * 256;        // K or V of one chunk: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes;     // K then V
 constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 128 B
-constexpr int kPBytes = 2 * kChunk * 16;       // 4 KB: two groups of 8 heads
+// P^T holds each probability as two rounded parts, hi = round(p) and
+// lo = round(p - hi), as separate groups of 8 columns: the PV MMA then sums
+// hi + lo in fp32, so rounding p to 16 bits costs about 2^-17 relative instead of
+// 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (N = 16, the columns are there anyway);
+// up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (N = 32).
+constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
 constexpr int kOffQ = kStages * kStageBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
@@ -68,7 +73,7 @@ constexpr int kOffRedMax = kOffBar + kNumBars * 8;
 constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
 constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
 constexpr int kSmemBytes = kOffMisc + 64;
-constexpr uint32_t kTmemCols = 64;             // S[2] at 0/16, O[2] at 32/48
+constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
 struct Bars {
   uint64_t* full;   // [kStages] K/V chunk landed (TMA tx)
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (lane == 0) {
       constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
       constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
-      constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, kN);
+      constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, GM <= 8 ? 16 : 32);
       const uint32_t ring = smem_addr(smem);
       const uint32_t qbase = smem_addr(smem + kOffQ);
       const uint32_t pbase = smem_addr(smem + kOffP);
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             for (int kk = 0; kk < kChunk / 16; ++kk) {
               const uint64_t ad = smem_desc(vbase + kk * 2 * kGroupBytes, 1024, kGroupBytes, kLayoutSwizzle128);
               const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
-              mma_f16(tmem + 32 + pb * 16, ad, bd, idesc_pv, kk > 0);
+              mma_f16(tmem + 32 + pb * 32, ad, bd, idesc_pv, kk > 0);
             }
             mma_commit(&bars.ofull[pb]);
             mma_commit(&bars.empty[st]);
@@ -404,13 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err)))
         return false;
       tc_fence_after();
-      float o[16];
-      tmem_load16(lane_base + 32 + pb * 16, o);
+      float o[16], olo[16];
+      tmem_load16(lane_base + 32 + pb * 32, o);
+      if (GM > 8) tmem_load16(lane_base + 32 + pb * 32 + 16, olo);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ofree[pb]);
 #pragma unroll
-      for (int h = 0; h < GM; ++h) acc[h] = pend_first ? o[h] : fmaf(acc[h], alpha_pend[h], o[h]);
+      for (int h = 0; h < GM; ++h) {
+        const float v = GM <= 8 ? o[h] + o[8 + h] : o[h] + olo[h];  // hi part + lo part
+        acc[h] = pend_first ? v : fmaf(acc[h], alpha_pend[h], v);
+      }
       if (pend_last) {
         const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G;
 #pragma unroll
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           ok = false;
           break;
         }
-        float pr[16];
+        float ph[16], pl[16];
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           const float* r = red_max + sb * 4 * kN + h;
@@ -477,18 +486,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const float mn = fmaxf(m[h], cm);
           alpha[h] = exp2f(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
           m[h] = mn;
-          pr[h] = h < G ? round_to<T>(exp2f(sv[h] - mn)) : 0.f;
-          lp[h] = fmaf(lp[h], alpha[h], pr[h]);
+          const float pe = h < G ? exp2f(sv[h] - mn) : 0.f;
+          ph[h] = round_to<T>(pe);
+          pl[h] = round_to<T>(pe - ph[h]);  // pe - ph[h] is exact in fp32
+          lp[h] = fmaf(lp[h], alpha[h], pe);
         }
 #pragma unroll
-        for (int h = GM; h < 16; ++h) pr[h] = 0.f;
-        // P^T for PV: token t's 16 head weights, MN-major without swizzle
+        for (int h = GM; h < 16; ++h) ph[h] = pl[h] = 0.f;
+        // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns a group
         unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
-        *reinterpret_cast<uint4*>(pdst) = make_uint4(pack2<T>(pr[0], pr[1]), pack2<T>(pr[2], pr[3]),
-                                                     pack2<T>(pr[4], pr[5]), pack2<T>(pr[6], pr[7]));
-        *reinterpret_cast<uint4*>(pdst + kChunk * 16) =
-            make_uint4(pack2<T>(pr[8], pr[9]), pack2<T>(pr[10], pr[11]), pack2<T>(pr[12], pr[13]),
-                       pack2<T>(pr[14], pr[15]));
+        auto put8 = [&](int group, const float* v) {
+          *reinterpret_cast<uint4*>(pdst + group * kChunk * 16) =
+              make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]), pack2<T>(v[6], v[7]));
+        };
+        if (GM <= 8) {
+          put8(0, ph);
+          put8(1, pl);
+        } else {
+          put8(0, ph);
+          put8(1, ph + 8);
+          put8(2, pl);
+          put8(3, pl + 8);
+        }
         // rows of the last loaded block past the context end: zero their V rows
         const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
         if (t >= rows_valid && t < rows_loaded) {
