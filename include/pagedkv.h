@@ -142,6 +142,29 @@ pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t m
                                 pkv_decode_plan* out);
 
 /*
+ * paged_block_swap_out / paged_block_swap_in -- preemption under memory pressure: move
+ * whole blocks (all KV heads and rows of K and V) between the pools and CPU memory, so
+ * a preempted sequence can be restored later and continue exactly where it stopped.
+ * Pages: "Paged Attention" glossary, paragraphs 3 and 5 (blocks of preempted sequences
+ * are evicted to CPU RAM and swapped back, generation resumes where it left off);
+ * "Efficient Memory Management ...", How It Works (preemption and swapping).
+ *
+ * block_ids: device int64 [num_ids].  host_k, host_v: [num_ids][num_kv_heads]
+ * [block_size][head_dim] in the cache dtype, in pinned (cudaHostAlloc /
+ * cudaHostRegister) host memory, or device memory; pageable memory is refused with
+ * PKV_ERR_INVALID_ARG.  swap_out copies pool block block_ids[i] to entry i; swap_in
+ * copies entry i into pool block block_ids[i].  Bit-exact.  Out-of-range ids set the
+ * device index flag and are skipped.  Stream-ordered like every other call: issue the
+ * swap-out before anything reuses the blocks.
+ */
+pkv_status paged_block_swap_out(const int64_t* block_ids, int32_t num_ids, const void* k_cache,
+                                const void* v_cache, void* host_k, void* host_v,
+                                const pkv_cache_desc* cache, void* stream);
+pkv_status paged_block_swap_in(const int64_t* block_ids, int32_t num_ids, const void* host_k,
+                               const void* host_v, void* k_cache, void* v_cache,
+                               const pkv_cache_desc* cache, void* stream);
+
+/*
  * Bytes of workspace paged_attention_decode needs for these sizes and config.  The
  * CUDA-core path needs none when every sequence fits one partition; the tensor-core
  * path always needs room for its work list (16 bytes per (sequence, KV head,
@@ -238,6 +261,7 @@ typedef struct {
   int64_t allocated_slots; /* used_blocks * block_size */
   int64_t max_len;         /* longest sequence */
   int64_t copies;          /* copy-on-write copies made so far */
+  int64_t swapped;         /* sequences swapped out (holding no blocks) */
 } pkv_block_stats;
 
 /* A manager for a pool of num_blocks blocks of block_size tokens.  Free with destroy. */
@@ -263,6 +287,21 @@ pkv_status pkv_bm_append(pkv_block_manager* manager, const int64_t* seq_ids, int
 
 /* The sequence finished: drop its references; blocks no longer referenced are freed. */
 pkv_status pkv_bm_free_sequence(pkv_block_manager* manager, int64_t seq_id);
+
+/*
+ * Preemption: *num_out = the sequence's blocks in logical order, copied to blocks_out
+ * (capacity entries), and the sequence drops its references (blocks nobody else
+ * holds become free).  The sequence stays known, with its length, as swapped out:
+ * copy those blocks out with paged_block_swap_out before anything reuses them.
+ */
+pkv_status pkv_bm_swap_out(pkv_block_manager* manager, int64_t seq_id, int32_t* blocks_out, int32_t capacity,
+                           int32_t* num_out);
+
+/* Restore a swapped-out sequence into fresh private blocks, listed in logical order;
+ * copy its data back into them with paged_block_swap_in.  PKV_ERR_OUT_OF_BLOCKS if
+ * the pool cannot hold it (nothing changes). */
+pkv_status pkv_bm_swap_in(pkv_block_manager* manager, int64_t seq_id, int32_t* blocks_out, int32_t capacity,
+                          int32_t* num_out);
 
 /* Rows of block_tables ([n][max_blocks], -1 padded) and context_lens for n sequences. */
 pkv_status pkv_bm_block_tables(const pkv_block_manager* manager, const int64_t* seq_ids, int32_t n,

@@ -33,6 +33,7 @@ class BlockManagerModel:
         self.filled = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.lens: dict[int, int] = {}
+        self.swapped: dict[int, int] = {}
         self.copies = 0
 
     def _take(self) -> int:
@@ -42,7 +43,7 @@ class BlockManagerModel:
         return b
 
     def add_sequence(self, seq: int, tokens: int) -> None:
-        assert seq not in self.tables
+        assert seq not in self.tables and seq not in self.swapped
         need = -(-tokens // self.block_size)
         if need > len(self.free):
             raise OutOfBlocks
@@ -54,7 +55,7 @@ class BlockManagerModel:
         self.tables[seq], self.lens[seq] = blocks, tokens
 
     def fork(self, parent: int, child: int) -> None:
-        assert child not in self.tables
+        assert child not in self.tables and child not in self.swapped
         for b in self.tables[parent]:
             self.refs[b] += 1
         self.tables[child] = list(self.tables[parent])
@@ -105,6 +106,23 @@ class BlockManagerModel:
                 self.free.append(b)
         del self.lens[seq]
 
+    def swap_out(self, seq: int) -> list[int]:
+        """Preempted: its blocks (to copy to CPU memory) are released; the length is kept."""
+        blocks = self.tables[seq]
+        n = self.lens[seq]
+        self.free_sequence(seq)
+        self.swapped[seq] = n
+        return blocks
+
+    def swap_in(self, seq: int) -> list[int]:
+        """Restored into fresh private blocks (to copy the saved data back into)."""
+        n = self.swapped[seq]
+        if -(-n // self.block_size) > len(self.free):
+            raise OutOfBlocks
+        del self.swapped[seq]
+        self.add_sequence(seq, n)
+        return list(self.tables[seq])
+
     def stats(self) -> dict:
         used = [b for b in range(self.num_blocks) if self.refs[b] > 0]
         return dict(num_blocks=self.num_blocks, free_blocks=len(self.free), used_blocks=len(used),
@@ -113,4 +131,4 @@ class BlockManagerModel:
                     stored_tokens=sum(self.filled[b] for b in used),
                     logical_tokens=sum(self.lens.values()),
                     allocated_slots=len(used) * self.block_size,
-                    max_len=max(self.lens.values(), default=0), copies=self.copies)
+                    max_len=max(self.lens.values(), default=0), copies=self.copies, swapped=len(self.swapped))

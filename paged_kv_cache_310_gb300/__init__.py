@@ -25,7 +25,7 @@ __all__ = [
     "PagedKVError", "CacheDesc", "DecodeConfig", "DecodePlan", "paged_attention_plan", "library", "library_path", "cache_desc",
     "paged_kv_append", "paged_block_copy", "paged_attention_decode",
     "paged_attention_workspace_bytes", "paged_attention_decode_no_alloc", "paged_attention_no_alloc_limit",
-    "paged_kv_gather", "device_error", "declared_functions",
+    "paged_kv_gather", "paged_block_swap_out", "paged_block_swap_in", "device_error", "declared_functions",
     "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
 ]
 
@@ -93,6 +93,8 @@ def library():
             "paged_attention_decode": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp, i32,
                                        vp, sz, desc_p, cfg_p, vp],
             "paged_kv_gather": [vp, vp, vp, i32, vp, i32, i32, vp, vp, desc_p, vp],
+            "paged_block_swap_out": [vp, i32, vp, vp, vp, vp, desc_p, vp],
+            "paged_block_swap_in": [vp, i32, vp, vp, vp, vp, desc_p, vp],
             "paged_attention_decode_no_alloc": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp,
                                                 i32, desc_p, cfg_p, vp],
             "paged_attention_no_alloc_limit": [],
@@ -171,6 +173,32 @@ def paged_block_copy(src_dst_pairs, k_cache, v_cache, host_pairs: torch.Tensor |
     n = src_dst_pairs.numel() // 2
     _check(library().paged_block_copy(_ptr(src_dst_pairs), _ptr(host_pairs), n, _ptr(k_cache),
                                       _ptr(v_cache), ctypes.byref(desc), _stream(k_cache)))
+
+
+def _swap_buffers(ids, k_cache, host_k, host_v):
+    _need_cuda(ids, k_cache)
+    if ids.dtype != torch.int64:
+        raise PagedKVError(1, "block ids must be int64")
+    shape = (ids.numel(),) + tuple(k_cache.shape[1:])
+    for h in (host_k, host_v):
+        if tuple(h.shape) != shape or h.dtype != k_cache.dtype or not h.is_contiguous():
+            raise PagedKVError(1, f"swap buffers must be contiguous {shape} in the cache dtype")
+
+
+def paged_block_swap_out(block_ids, k_cache, v_cache, host_k, host_v) -> None:
+    """host_k/v[i] <- pool block block_ids[i] (device int64 ids; pinned host buffers)."""
+    _swap_buffers(block_ids, k_cache, host_k, host_v)
+    desc = cache_desc(k_cache)
+    _check(library().paged_block_swap_out(_ptr(block_ids), block_ids.numel(), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(host_k), _ptr(host_v), ctypes.byref(desc), _stream(k_cache)))
+
+
+def paged_block_swap_in(block_ids, host_k, host_v, k_cache, v_cache) -> None:
+    """pool block block_ids[i] <- host_k/v[i]."""
+    _swap_buffers(block_ids, k_cache, host_k, host_v)
+    desc = cache_desc(k_cache)
+    _check(library().paged_block_swap_in(_ptr(block_ids), block_ids.numel(), _ptr(host_k), _ptr(host_v),
+                                         _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _stream(k_cache)))
 
 
 def _config(path: int, partition_tokens: int) -> DecodeConfig:

@@ -19,7 +19,8 @@ class BlockStats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32),
                 ("num_sequences", ctypes.c_int32), ("shared_blocks", ctypes.c_int32),
                 ("stored_tokens", ctypes.c_int64), ("logical_tokens", ctypes.c_int64),
-                ("allocated_slots", ctypes.c_int64), ("max_len", ctypes.c_int64), ("copies", ctypes.c_int64)]
+                ("allocated_slots", ctypes.c_int64), ("max_len", ctypes.c_int64), ("copies", ctypes.c_int64),
+                ("swapped", ctypes.c_int64)]
 
 
 def _lib():
@@ -35,8 +36,11 @@ def _lib():
         lib.pkv_bm_free_sequence.argtypes = [vp, i64]
         lib.pkv_bm_block_tables.argtypes = [vp, vp, i32, i32, vp, vp]
         lib.pkv_bm_stats.argtypes = [vp, ctypes.POINTER(BlockStats)]
+        lib.pkv_bm_swap_out.argtypes = [vp, i64, vp, i32, ctypes.POINTER(i32)]
+        lib.pkv_bm_swap_in.argtypes = [vp, i64, vp, i32, ctypes.POINTER(i32)]
         for n in ("pkv_bm_create", "pkv_bm_add_sequence", "pkv_bm_fork", "pkv_bm_append",
-                  "pkv_bm_free_sequence", "pkv_bm_block_tables", "pkv_bm_stats"):
+                  "pkv_bm_free_sequence", "pkv_bm_block_tables", "pkv_bm_stats", "pkv_bm_swap_out",
+                  "pkv_bm_swap_in"):
             getattr(lib, n).restype = ctypes.c_int
         lib._bm_bound = True
     return lib
@@ -82,6 +86,21 @@ class BlockManager:
 
     def free_sequence(self, seq_id: int) -> None:
         _check(self._lib.pkv_bm_free_sequence(self._h, seq_id))
+
+    def _blocks_call(self, fn, seq_id):
+        cap = self.num_blocks
+        out = torch.empty(cap, dtype=torch.int32)
+        n = ctypes.c_int32(0)
+        _check(fn(self._h, seq_id, out.data_ptr(), cap, ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+    def swap_out(self, seq_id: int) -> list:
+        """Preempt: the sequence's blocks (copy them out with paged_block_swap_out), released."""
+        return self._blocks_call(self._lib.pkv_bm_swap_out, seq_id)
+
+    def swap_in(self, seq_id: int) -> list:
+        """Restore into fresh blocks (copy the data back with paged_block_swap_in)."""
+        return self._blocks_call(self._lib.pkv_bm_swap_in, seq_id)
 
     def block_tables(self, seq_ids, max_blocks: int | None = None):
         """(block_tables int32 [n, max_blocks] padded with -1, context_lens int32 [n])."""

@@ -269,6 +269,63 @@ pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t m
   return PKV_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// A pointer the device can use for `host`: pinned or registered host memory (its
+// device alias), device or managed memory (as is).  Pageable memory is refused.
+pkv_status device_view(const void* host, void** out) {
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, host);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(PKV_ERR_INVALID_ARG, "swap buffer: not memory CUDA knows (%s)", cudaGetErrorString(e));
+  }
+  if (attr.type == cudaMemoryTypeUnregistered)
+    return fail(PKV_ERR_INVALID_ARG, "swap buffer is pageable host memory: pin it (cudaHostAlloc / cudaHostRegister)");
+  *out = attr.type == cudaMemoryTypeHost ? attr.devicePointer : const_cast<void*>(host);
+  if (!*out) return fail(PKV_ERR_INVALID_ARG, "swap buffer has no device mapping");
+  return PKV_OK;
+}
+
+pkv_status swap(bool out, const int64_t* ids, int32_t n, void* k_cache, void* v_cache, const void* stage_k,
+                const void* stage_v, const pkv_cache_desc* cache, void* stream) {
+  if (pkv_status st = check_cache(cache)) return st;
+  if (n < 0 || n > 65535) return fail(PKV_ERR_INVALID_ARG, "num_ids %d outside [0, 65535]", n);
+  if (n == 0) return PKV_OK;
+  if (!ids || !k_cache || !v_cache || !stage_k || !stage_v) return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(stage_k) || !aligned16(stage_v))
+    return fail(PKV_ERR_INVALID_ARG, "caches and swap buffers must be 16-byte aligned");
+  void *dk = nullptr, *dv = nullptr;
+  if (pkv_status st = device_view(stage_k, &dk)) return st;
+  if (pkv_status st = device_view(stage_v, &dv)) return st;
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  const int64_t block_bytes = static_cast<int64_t>(cache->num_kv_heads) * cache->block_size *
+                              cache->head_dim * elem_bytes(cache->dtype);
+  cudaError_t e = launch_swap(out, ids, n, k_cache, v_cache, dk, dv, block_bytes, cache->num_blocks, flag,
+                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "swap launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_block_swap_out(const int64_t* block_ids, int32_t num_ids, const void* k_cache,
+                                const void* v_cache, void* host_k, void* host_v,
+                                const pkv_cache_desc* cache, void* stream) {
+  return swap(true, block_ids, num_ids, const_cast<void*>(k_cache), const_cast<void*>(v_cache), host_k, host_v,
+              cache, stream);
+}
+
+pkv_status paged_block_swap_in(const int64_t* block_ids, int32_t num_ids, const void* host_k,
+                               const void* host_v, void* k_cache, void* v_cache,
+                               const pkv_cache_desc* cache, void* stream) {
+  return swap(false, block_ids, num_ids, k_cache, v_cache, host_k, host_v, cache, stream);
+}
+
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t max_context_len, const pkv_cache_desc* cache,
                                        const pkv_decode_config* config) {

@@ -35,6 +35,7 @@ struct pkv_block_manager {
     int64_t len = 0;
   };
   std::unordered_map<int64_t, Seq> seqs;
+  std::unordered_map<int64_t, int64_t> swapped;  // swapped-out sequence -> length
   int64_t copies = 0;  // copy-on-write copies made so far
 };
 
@@ -82,7 +83,8 @@ void pkv_bm_destroy(pkv_block_manager* m) { delete m; }
 pkv_status pkv_bm_add_sequence(pkv_block_manager* m, int64_t seq_id, int64_t num_tokens) {
   if (!m) return err(PKV_ERR_INVALID_ARG, "manager is NULL");
   if (num_tokens < 0) return err(PKV_ERR_INVALID_ARG, "num_tokens < 0");
-  if (m->seqs.count(seq_id)) return err(PKV_ERR_INVALID_ARG, "sequence id already present");
+  if (m->seqs.count(seq_id) || m->swapped.count(seq_id))
+    return err(PKV_ERR_INVALID_ARG, "sequence id already present");
   const int64_t need = blocks_for(num_tokens, m->block_size);
   if (need > static_cast<int64_t>(m->free_stack.size()))
     return err(PKV_ERR_OUT_OF_BLOCKS, "not enough free blocks for the prompt");
@@ -101,7 +103,7 @@ pkv_status pkv_bm_fork(pkv_block_manager* m, int64_t parent, int64_t child) {
   if (!m) return err(PKV_ERR_INVALID_ARG, "manager is NULL");
   auto it = m->seqs.find(parent);
   if (it == m->seqs.end()) return err(PKV_ERR_INVALID_ARG, "unknown parent sequence");
-  if (m->seqs.count(child)) return err(PKV_ERR_INVALID_ARG, "child id already present");
+  if (m->seqs.count(child) || m->swapped.count(child)) return err(PKV_ERR_INVALID_ARG, "child id already present");
   const auto copy = it->second;  // the child shares every physical block by reference
   for (int32_t b : copy.blocks) ++m->refcount[b];
   m->seqs[child] = copy;
@@ -175,6 +177,46 @@ pkv_status pkv_bm_free_sequence(pkv_block_manager* m, int64_t seq_id) {
   return PKV_OK;
 }
 
+pkv_status pkv_bm_swap_out(pkv_block_manager* m, int64_t seq_id, int32_t* blocks_out, int32_t capacity,
+                           int32_t* num_out) {
+  if (!m || !num_out) return err(PKV_ERR_INVALID_ARG, "NULL argument");
+  auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return err(PKV_ERR_INVALID_ARG, "unknown (or already swapped) sequence id");
+  const auto& blocks = it->second.blocks;
+  if (static_cast<int64_t>(blocks.size()) > capacity || (!blocks.empty() && !blocks_out))
+    return err(PKV_ERR_INVALID_ARG, "blocks_out too small");
+  for (size_t i = 0; i < blocks.size(); ++i) blocks_out[i] = blocks[i];
+  *num_out = static_cast<int32_t>(blocks.size());
+  const int64_t len = it->second.len;
+  for (auto b = blocks.rbegin(); b != blocks.rend(); ++b) release_block(m, *b);
+  m->seqs.erase(it);
+  m->swapped[seq_id] = len;
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_swap_in(pkv_block_manager* m, int64_t seq_id, int32_t* blocks_out, int32_t capacity,
+                          int32_t* num_out) {
+  if (!m || !num_out) return err(PKV_ERR_INVALID_ARG, "NULL argument");
+  auto it = m->swapped.find(seq_id);
+  if (it == m->swapped.end()) return err(PKV_ERR_INVALID_ARG, "sequence is not swapped out");
+  const int64_t len = it->second;
+  const int64_t need = blocks_for(len, m->block_size);
+  if (need > capacity || (need > 0 && !blocks_out)) return err(PKV_ERR_INVALID_ARG, "blocks_out too small");
+  if (need > static_cast<int64_t>(m->free_stack.size()))
+    return err(PKV_ERR_OUT_OF_BLOCKS, "not enough free blocks to swap the sequence in");
+  auto& s = m->seqs[seq_id];
+  for (int64_t i = 0; i < need; ++i) {
+    const int32_t b = take_block(m);
+    m->filled[b] = static_cast<int32_t>(std::min<int64_t>(m->block_size, len - i * m->block_size));
+    s.blocks.push_back(b);
+    blocks_out[i] = b;
+  }
+  s.len = len;
+  *num_out = static_cast<int32_t>(need);
+  m->swapped.erase(it);
+  return PKV_OK;
+}
+
 pkv_status pkv_bm_block_tables(const pkv_block_manager* m, const int64_t* seq_ids, int32_t n,
                                int32_t max_blocks, int32_t* tables, int32_t* lens) {
   if (!m || (n > 0 && (!seq_ids || !tables || !lens))) return err(PKV_ERR_INVALID_ARG, "NULL argument");
@@ -212,6 +254,7 @@ pkv_status pkv_bm_stats(const pkv_block_manager* m, pkv_block_stats* out) {
   }
   st.allocated_slots = static_cast<int64_t>(st.used_blocks) * m->block_size;
   st.copies = m->copies;
+  st.swapped = static_cast<int64_t>(m->swapped.size());
   *out = st;
   return PKV_OK;
 }

@@ -107,6 +107,34 @@ gather_kernel(const uint4* __restrict__ kc, const uint4* __restrict__ vc,
   }
 }
 
+// Swap: whole blocks (all heads and rows of K and V) between the pools and a staging
+// buffer of [n][block] in memory the device can reach (pinned host memory for a real
+// swap).  blockIdx.y = listed block, x strides over its 16-byte vectors.
+template <bool kOut>
+__global__ void __launch_bounds__(kThreads)
+swap_kernel(const int64_t* __restrict__ ids, uint4* kc, uint4* vc, uint4* hk, uint4* hv, int64_t block_vecs,
+            int32_t num_blocks, int* err) {
+  const int64_t b = ids[blockIdx.y];
+  if (b < 0 || b >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(err, kErrIndex);
+    return;
+  }
+  uint4* pk = kc + b * block_vecs;
+  uint4* pv = vc + b * block_vecs;
+  uint4* sk = hk + static_cast<int64_t>(blockIdx.y) * block_vecs;
+  uint4* sv = hv + static_cast<int64_t>(blockIdx.y) * block_vecs;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < block_vecs;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (kOut) {
+      sk[i] = pk[i];
+      sv[i] = pv[i];
+    } else {
+      pk[i] = sk[i];
+      pv[i] = sv[i];
+    }
+  }
+}
+
 // Self-test of the bounded wait: an mbarrier that expects one arrival nobody makes.
 // The wait gives up after limit_ns, sets the timeout flag and the kernel returns.
 __global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
@@ -120,6 +148,22 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
 }
 
 }  // namespace
+
+cudaError_t launch_swap(bool out, const int64_t* ids, int32_t n, void* k_cache, void* v_cache, void* stage_k,
+                        void* stage_v, int64_t block_bytes, int32_t num_blocks, int* err, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t block_vecs = block_bytes / 16;
+  dim3 grid(grid_for(block_vecs, 64), n);
+  auto* kc = static_cast<uint4*>(k_cache);
+  auto* vc = static_cast<uint4*>(v_cache);
+  auto* sk = static_cast<uint4*>(stage_k);
+  auto* sv = static_cast<uint4*>(stage_v);
+  if (out)
+    swap_kernel<true><<<grid, kThreads, 0, stream>>>(ids, kc, vc, sk, sv, block_vecs, num_blocks, err);
+  else
+    swap_kernel<false><<<grid, kThreads, 0, stream>>>(ids, kc, vc, sk, sv, block_vecs, num_blocks, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream) {
   wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err);

@@ -43,6 +43,10 @@ cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Records a failure message for paged_kv_last_error() on this host thread.
 pkv_status record_error(pkv_status status, const char* message);
 
+// Swap whole blocks between the pools and a device-reachable staging buffer.
+cudaError_t launch_swap(bool out, const int64_t* ids, int32_t n, void* k_cache, void* v_cache, void* stage_k,
+                        void* stage_v, int64_t block_bytes, int32_t num_blocks, int* err, cudaStream_t stream);
+
 // Diagnostic: one bounded wait that cannot complete (see paged_kv_selftest_wait_timeout).
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int* err, cudaStream_t stream);
 

@@ -58,6 +58,23 @@ def test_random_operations_match_the_model(seed):
             model.fork(parent, next_id)
             bm.fork(parent, next_id)
             next_id += 1
+        elif op < 0.45 and (live or model.swapped):
+            if model.swapped and rng.random() < 0.5:
+                s = rng.choice(sorted(model.swapped))
+                try:
+                    want = model.swap_in(s)
+                    ok = True
+                except OutOfBlocks:
+                    ok = False
+                if ok:
+                    assert bm.swap_in(s) == want
+                else:
+                    with pytest.raises(PagedKVError) as e:
+                        bm.swap_in(s)
+                    assert e.value.status == 7
+            elif live:
+                s = rng.choice(live)
+                assert bm.swap_out(s) == model.swap_out(s)
         elif op < 0.85:
             seqs = rng.sample(live, rng.randint(1, len(live)))
             try:
