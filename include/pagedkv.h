@@ -80,7 +80,8 @@ typedef struct {
   int32_t dtype;        /* pkv_dtype of the caches, q, k and v */
 } pkv_cache_desc;
 
-/* Decode path selection and split-K partition size (NULL config = automatic). */
+/* Decode path selection and split-K partition size (NULL config = automatic: tensor
+ * cores for f16/bf16 with head_dim 128 and groups <= 16, CUDA cores otherwise). */
 typedef enum { PKV_PATH_AUTO = 0, PKV_PATH_CUDA_CORE = 1, PKV_PATH_TENSOR_CORE = 2 } pkv_path;
 
 typedef struct {

@@ -132,9 +132,12 @@ def test_plan_reports_path_partitions_and_launches(lib):
     p = pkv.paged_attention_plan(128, 64, 4096, k16)            # GQA group 8 -> tensor cores
     assert p["path"] == pkv.PATH_TENSOR_CORE and p["partition_tokens"] % 128 == 0
     assert p["partition_tokens"] <= 4096 and p["kernel_launches"] == 2 + (p["max_partitions"] > 1)
-    p1 = pkv.paged_attention_plan(64, 8, 2048, k16)             # group 1 -> CUDA cores, 512-token partitions
+    p1 = pkv.paged_attention_plan(64, 8, 2048, k16, path=pkv.PATH_CUDA_CORE)   # 512-token partitions
     assert p1["path"] == pkv.PATH_CUDA_CORE and p1["partition_tokens"] == 512 and p1["max_partitions"] == 4
     assert p1["kernel_launches"] == 2
-    assert pkv.paged_attention_plan(64, 8, 300, k16)["kernel_launches"] == 1   # one partition, no merge
+    assert pkv.paged_attention_plan(64, 8, 300, k16, path=pkv.PATH_CUDA_CORE)["kernel_launches"] == 1
+    assert pkv.paged_attention_plan(64, 8, 2048, k16)["path"] == pkv.PATH_TENSOR_CORE  # automatic, bf16 D128
+    k32 = __import__("torch").empty((1, 8, 16, 64), dtype=__import__("torch").float32)
+    assert pkv.paged_attention_plan(64, 8, 2048, k32)["path"] == pkv.PATH_CUDA_CORE   # f32, D64
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_attention_plan(64, 8, 2048, k16, path=pkv.PATH_TENSOR_CORE, partition_tokens=8192)
