@@ -53,6 +53,31 @@ def parse():
     return ap.parse_args()
 
 
+KERNEL_SOURCES = {"tensor_core": ["common.cuh", "decode_tc.cu", "launch.h", "tcgen05.cuh"],
+                  "cuda_core": ["common.cuh", "decode_simt.cu", "launch.h"]}
+
+
+def recorded_traffic(path_name, workload, partition):
+    """DRAM bytes per launch from a committed ncu capture of the same kernel sources,
+    workload and partition size (profiles/traffic.json), else None."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entries = json.load(f)["entries"]
+        h = hashlib.sha256()
+        for name in KERNEL_SOURCES[path_name]:
+            with open(os.path.join(ROOT, "paged_kv_cache_310_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    for e in entries:
+        if (e.get("path") == path_name and e.get("workload") == workload and e.get("partition_tokens") == partition
+                and e.get("sources_sha256") == sha):
+            return e["dram_bytes_per_launch"]
+    return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -317,8 +342,10 @@ def main():
         "seq_tokens_per_s": world * tokens / (ms_per_step * 1e-3),
         "hbm_frac_step": (algo_bytes / (ms_per_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                     "kernel": "paged_attention_decode (partition kernel + merge)",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": recorded_traffic({1: "cuda_core", 2: "tensor_core"}[plan["path"]], w.name,
+                                                 plan["partition_tokens"]),
+                     "kernel": "paged_attention_decode (work list + decode_tc, or decode_simt + merge)",
                      "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": decode_ms},
         "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
