@@ -14,6 +14,8 @@ What each function computes, and where the pages state it:
   K/V gathered through its block table ("anthology-of-the-sota note-023", Method and
   Concepts; "Paged Attention" glossary, paragraph 4: the attention arithmetic is
   unchanged, only where K/V live).
+* :func:`attention_prefill` -- several new tokens per sequence with a causal mask
+  (prefill / chunked prefill); one new token is exactly decode.
 * :func:`attention_partitions` / :func:`merge_partitions` -- the same softmax over
   consecutive token ranges and their exact recombination.  Not on the pages; it is
   the split over context partitions that long sequences need, pinned against the
@@ -82,10 +84,12 @@ def _load():
             lib.pkvo_attention_partitions.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                                       i32, i32, i32, dbl, i32, i32, vp, vp, vp]
             lib.pkvo_merge_partitions.argtypes = [vp, vp, vp, i64, i32, i32, vp]
+            lib.pkvo_attention_prefill.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                                   i32, i32, dbl, i32, vp]
             lib.pkvo_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32]
             lib.pkvo_block_copy.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32]
             lib.pkvo_gather.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp]
-            for name in ("pkvo_decode", "pkvo_attention_decode", "pkvo_attention_partitions",
+            for name in ("pkvo_decode", "pkvo_attention_decode", "pkvo_attention_partitions", "pkvo_attention_prefill",
                          "pkvo_merge_partitions", "pkvo_kv_append", "pkvo_block_copy", "pkvo_gather"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -137,6 +141,29 @@ def attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, num
                                        cl.data_ptr(), S, Hq, Hkv, D, bs, NB, float(scale),
                                        int(num_threads), out.ctypes.data)
     _check(rc, "attention_decode")
+    return out
+
+
+def attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, num_threads=0):
+    """float64 [T, Hq, D]: causal attention of each sequence's new tokens.
+
+    Sequence s's new tokens are rows query_start[s]..query_start[s+1]-1 of q and the last
+    (query_start[s+1] - query_start[s]) of its context_lens[s] tokens; the token at
+    position p attends to positions 0..p.
+    """
+    q, k_cache, v_cache = _cpu(q), _cpu(k_cache, q.dtype), _cpu(v_cache, q.dtype)
+    bt, cl = _cpu(block_tables, torch.int32), _cpu(context_lens, torch.int32)
+    qs = _cpu(query_start, torch.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    S = cl.numel()
+    if qs.numel() != S + 1 or int(qs[-1]) != T:
+        raise ValueError("query_start must be [S+1] ending at the number of query rows")
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = _load().pkvo_attention_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), DTYPE_CODE[q.dtype],
+                                        bt.data_ptr(), bt.shape[1], cl.data_ptr(), qs.data_ptr(), S, Hq, Hkv, D, bs,
+                                        NB, float(scale), int(num_threads), out.ctypes.data)
+    _check(rc, "attention_prefill")
     return out
 
 

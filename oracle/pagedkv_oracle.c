@@ -116,19 +116,19 @@ static int64_t orc_lookup(const orc_pool* p, const int32_t* tables, int32_t max_
 }
 
 /*
- * Attention of one (sequence s, query head h) over tokens [t0, t1) of the sequence:
+ * Attention of one query row (element offset qoff in q: the vector of sequence s,
+ * query head h) over tokens [t0, t1) of the sequence:
  * scores s_j = scale * sum_d q[d] K_j[d]; m = max_j s_j; w_j = exp(s_j - m);
  * l = sum_j w_j; o[d] = sum_j w_j V_j[d] (NOT divided by l).  Returns ORC_OK or
  * ORC_BAD_INDEX.  For t1 <= t0: m = -inf, l = 0, o = 0.
  */
-static int orc_head(const orc_pool* p, const void* q, const void* kc, const void* vc,
+static int orc_head(const orc_pool* p, const void* q, size_t qoff, const void* kc, const void* vc,
                     const int32_t* tables, int32_t max_blocks, int32_t num_q_heads, int32_t s,
                     int32_t h, int32_t t0, int32_t t1, double scale, double* scores, double* m_out,
                     double* l_out, double* o) {
     const int32_t D = p->head_dim;
     const int32_t G = num_q_heads / p->num_kv_heads;
     const int32_t g = h / G;
-    const size_t qoff = ((size_t)s * num_q_heads + h) * D;
     for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
     if (t1 <= t0) {
         *m_out = -INFINITY;
@@ -207,14 +207,75 @@ int pkvo_attention_decode(const void* q, const void* k_cache, const void* v_cach
                 status = ORC_NO_MEMORY;
                 continue;
             }
-            int rc = orc_head(&p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                              num_q_heads, s, h, 0, context_lens[s], scale, scores, &m, &l, o);
+            int rc = orc_head(&p, q, (size_t)i * head_dim, k_cache, v_cache, block_tables,
+                              max_blocks_per_seq, num_q_heads, s, h, 0, context_lens[s], scale,
+                              scores, &m, &l, o);
             if (rc != ORC_OK) {
                 status = rc;
                 continue;
             }
             if (context_lens[s] > 0)
                 for (int32_t d = 0; d < head_dim; ++d) o[d] /= l;
+        }
+        free(scores);
+    }
+    return status;
+}
+
+/*
+ * Multi-token attention with a causal mask (prefill, chunked prefill): sequence s
+ * brings n_s = query_start[s+1] - query_start[s] new tokens, the last n_s of its
+ * context_lens[s] tokens (their K/V already written to the pool).  New token i sits
+ * at position p = context_lens[s] - n_s + i and attends to tokens 0..p only.
+ * q, out: [T][Hq][D], T = query_start[num_seqs]; sequence s's rows start at
+ * query_start[s].  One new token per sequence is exactly decode.
+ */
+int pkvo_attention_prefill(const void* q, const void* k_cache, const void* v_cache, int32_t dtype,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* context_lens, const int32_t* query_start,
+                           int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale,
+                           int32_t num_threads, double* out) {
+    orc_pool p = {num_blocks, num_kv_heads, block_size, head_dim, dtype};
+    if (!orc_pool_ok(&p) || num_seqs < 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads ||
+        !query_start || (num_seqs && (!q || !k_cache || !v_cache || !context_lens || !out)))
+        return ORC_BAD_ARG;
+    int32_t max_len = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t n = query_start[s + 1] - query_start[s];
+        if (n < 0 || context_lens[s] < n) return ORC_BAD_ARG;
+        if (context_lens[s] > max_len) max_len = context_lens[s];
+    }
+    const int64_t rows = (int64_t)query_start[num_seqs] * num_q_heads;
+    int status = ORC_OK;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(orc_threads(num_threads))
+#endif
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        double m, l;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 8)
+#endif
+        for (int64_t r = 0; r < rows; ++r) {
+            const int32_t t = (int32_t)(r / num_q_heads), h = (int32_t)(r % num_q_heads);
+            int32_t s = 0;
+            while (query_start[s + 1] <= t) ++s;  /* the sequence owning token row t */
+            const int32_t n = query_start[s + 1] - query_start[s];
+            const int32_t pos = context_lens[s] - n + (t - query_start[s]);
+            double* o = out + (size_t)r * head_dim;
+            if (!scores) {
+                status = ORC_NO_MEMORY;
+                continue;
+            }
+            int rc = orc_head(&p, q, (size_t)r * head_dim, k_cache, v_cache, block_tables,
+                              max_blocks_per_seq, num_q_heads, s, h, 0, pos + 1, scale, scores, &m,
+                              &l, o);
+            if (rc != ORC_OK) {
+                status = rc;
+                continue;
+            }
+            for (int32_t d = 0; d < head_dim; ++d) o[d] /= l;
         }
         free(scores);
     }
@@ -248,9 +309,9 @@ int pkvo_attention_partitions(const void* q, const void* k_cache, const void* v_
                 size_t k = ((size_t)s * num_q_heads + h) * max_parts + pi;
                 int32_t t0 = pi * part_tokens;
                 int32_t t1 = t0 + part_tokens < n ? t0 + part_tokens : n;
-                status = orc_head(&p, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                  num_q_heads, s, h, t0, t1, scale, scores, &m_out[k], &l_out[k],
-                                  o_out + k * head_dim);
+                status = orc_head(&p, q, ((size_t)s * num_q_heads + h) * head_dim, k_cache,
+                                  v_cache, block_tables, max_blocks_per_seq, num_q_heads, s, h, t0,
+                                  t1, scale, scores, &m_out[k], &l_out[k], o_out + k * head_dim);
             }
     }
     free(scores);

@@ -2,7 +2,7 @@
 
 Each case plants one mistake in a copy of oracle/pagedkv_oracle.c (a wrong index, a
 dropped term, a transposed operand, a flipped sign), builds the copy separately, and
-runs the pin suite against it in a child process: the suite must fail.  The oracle
+runs the pin suites (decode and prefill) against it in a child process: they must fail.  The oracle
 itself is never modified.
 """
 import os
@@ -23,8 +23,12 @@ MUTATIONS = {
                      "size_t row = orc_row(p, b, g, p->block_size - 1 - j % p->block_size);"),
     "exp_sign": ("double w = exp(scores[j - t0] - m);", "double w = exp(m - scores[j - t0]);"),
     "normalisation_dropped": ("for (int32_t d = 0; d < head_dim; ++d) o[d] /= l;", "(void)l;"),
-    "last_token_dropped": ("num_q_heads, s, h, 0, context_lens[s], scale, scores, &m, &l, o);",
-                           "num_q_heads, s, h, 0, context_lens[s] - (context_lens[s] > 1), scale, scores, &m, &l, o);"),
+    "last_token_dropped": ("num_q_heads, s, h, 0, context_lens[s], scale,",
+                           "num_q_heads, s, h, 0, context_lens[s] - (context_lens[s] > 1), scale,"),
+    "causal_diagonal_dropped": ("max_blocks_per_seq, num_q_heads, s, h, 0, pos + 1, scale,",
+                                "max_blocks_per_seq, num_q_heads, s, h, 0, pos + (pos == 0), scale,"),
+    "prefill_position_from_start": ("const int32_t pos = context_lens[s] - n + (t - query_start[s]);",
+                                    "const int32_t pos = t - query_start[s];"),
     "merge_weight_sign": ("double c = exp(m[pi] - M);", "double c = exp(M - m[pi]);"),
     "append_row_zero": ("int32_t r = (int32_t)(slot % block_size);", "int32_t r = 0;"),
     "copy_k_only": ("memcpy((char*)v_cache + dst * block_bytes, (const char*)v_cache + src * block_bytes, block_bytes);", ""),
@@ -44,6 +48,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", str(mutant_src), "-o",
                     str(lib), "-lm"], check=True, capture_output=True)
     env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_oracle_pins.py"), "-x", "-q",
-                        "-p", "no:cacheprovider"], env=env, capture_output=True, text=True, timeout=600)
+    pins = [os.path.join(HERE, f) for f in ("test_oracle_pins.py", "test_oracle_prefill_pins.py")]
+    r = subprocess.run([sys.executable, "-m", "pytest", *pins, "-x", "-q", "-p", "no:cacheprovider"], env=env,
+                       capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"the pins did not notice the '{name}' mutation:\n{r.stdout[-2000:]}"
