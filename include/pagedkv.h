@@ -230,6 +230,33 @@ pkv_status paged_attention_decode_no_alloc(const void* q, const void* k_cache, c
 size_t paged_attention_no_alloc_limit(void);
 
 /*
+ * paged_attention_prefill -- several new tokens per sequence (prefill, chunked prefill)
+ * attending through block tables with a causal mask.
+ * Pages: note-023, Method (attention gathers K/V through the block table) and Open
+ * questions (chunked prefill); attention arithmetic unchanged ("Paged Attention"
+ * glossary, paragraph 4).
+ *
+ * Sequence s brings n_s = query_start[s+1] - query_start[s] new tokens: rows
+ * query_start[s] .. query_start[s+1]-1 of q and out ([num_query_tokens][Hq][D]),
+ * the last n_s of its context_lens[s] tokens, whose K/V are already in the pool
+ * (paged_kv_append first).  New token i at position p = context_lens[s] - n_s + i:
+ *   out[row][h] = sum_{j <= p} softmax_j(scale * q[row][h] . K_j) V_j.
+ * query_start: device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0 and
+ * query_start[num_seqs] = num_query_tokens.  A sequence with n_s > context_lens[s]
+ * or context_lens[s] > max_context_len sets the device index flag and is skipped.
+ * Tensor cores only: f16/bf16, head_dim 128, query-head groups <= 16.  workspace:
+ * at least paged_attention_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+size_t paged_attention_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_query_tokens,
+                                               const pkv_cache_desc* cache);
+pkv_status paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_query_tokens, int32_t max_context_len,
+                                   float scale, void* out, int32_t out_dtype, void* workspace,
+                                   size_t workspace_bytes, const pkv_cache_desc* cache, void* stream);
+
+/*
  * paged_kv_gather -- the block-table lookup alone (testing the indexing bit-exactly):
  * k_out[s][h][j][:] = k_cache[block_tables[s][j / bs]][h][j % bs][:] for j < n_s,
  * same for v.  Rows j >= context_lens[s] are not written.

@@ -25,7 +25,7 @@ __all__ = [
     "PagedKVError", "CacheDesc", "DecodeConfig", "DecodePlan", "paged_attention_plan", "library", "library_path", "cache_desc",
     "paged_kv_append", "paged_block_copy", "paged_attention_decode",
     "paged_attention_workspace_bytes", "paged_attention_decode_no_alloc", "paged_attention_no_alloc_limit",
-    "paged_kv_gather", "paged_block_swap_out", "paged_block_swap_in", "device_error", "declared_functions",
+    "paged_kv_gather", "paged_block_swap_out", "paged_block_swap_in", "paged_attention_prefill", "device_error", "declared_functions",
     "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
 ]
 
@@ -94,6 +94,9 @@ def library():
                                        vp, sz, desc_p, cfg_p, vp],
             "paged_kv_gather": [vp, vp, vp, i32, vp, i32, i32, vp, vp, desc_p, vp],
             "paged_block_swap_out": [vp, i32, vp, vp, vp, vp, desc_p, vp],
+            "paged_attention_prefill": [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, i32,
+                                        vp, sz, desc_p, vp],
+            "paged_attention_prefill_workspace_bytes": [i32, i32, i32, desc_p],
             "paged_block_swap_in": [vp, i32, vp, vp, vp, vp, desc_p, vp],
             "paged_attention_decode_no_alloc": [vp, vp, vp, vp, i32, vp, i32, i32, i32, ctypes.c_float, vp,
                                                 i32, desc_p, cfg_p, vp],
@@ -109,6 +112,7 @@ def library():
             fn.restype = ctypes.c_int
         lib.paged_attention_workspace_bytes.restype = sz
         lib.paged_attention_no_alloc_limit.restype = sz
+        lib.paged_attention_prefill_workspace_bytes.restype = sz
         lib.paged_kv_last_error.restype = ctypes.c_char_p
         lib.paged_kv_version.restype = ctypes.c_char_p
         _lib = lib
@@ -303,6 +307,41 @@ def paged_attention_decode_no_alloc(q, k_cache, v_cache, block_tables, context_l
 def paged_attention_no_alloc_limit() -> int:
     """Bytes of the built-in workspace array used by paged_attention_decode_no_alloc."""
     return int(library().paged_attention_no_alloc_limit())
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, out, *,
+                            max_context_len: int | None = None,
+                            workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Causal attention of several new tokens per sequence (prefill / chunked prefill).
+
+    q, out [T, Hq, D]: sequence s's new tokens are rows query_start[s]..query_start[s+1]-1,
+    the last ones of its context_lens[s] tokens (K/V already appended).  query_start:
+    int32 [S+1] on the device.
+    """
+    _need_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start, out, workspace)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or query_start.dtype != torch.int32:
+        raise PagedKVError(1, "block_tables, context_lens and query_start must be int32")
+    if q.dim() != 3 or out.shape != q.shape or q.dtype != k_cache.dtype or q.shape[2] != k_cache.shape[3]:
+        raise PagedKVError(1, "shape/dtype mismatch between q, out and the caches")
+    T, Hq, _ = q.shape
+    S = context_lens.numel()
+    if query_start.numel() != S + 1 or block_tables.shape[0] != S:
+        raise PagedKVError(1, "query_start must be [S+1] and block_tables [S, max_blocks]")
+    if out.dtype not in DTYPE_CODE:
+        raise PagedKVError(2, f"out dtype {out.dtype}")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max()) if S else 0
+    desc = cache_desc(k_cache)
+    lib = library()
+    need = int(lib.paged_attention_prefill_workspace_bytes(S, Hq, T, ctypes.byref(desc)))
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_attention_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(context_lens), _ptr(query_start), S, Hq, T,
+                                       max_context_len, float(scale), _ptr(out), DTYPE_CODE[out.dtype],
+                                       _ptr(workspace), ws_bytes, ctypes.byref(desc), _stream(q)))
+    return out
 
 
 def paged_kv_gather(k_cache, v_cache, block_tables, context_lens, k_out, v_out, *,

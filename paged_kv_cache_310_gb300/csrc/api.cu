@@ -408,6 +408,78 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   return PKV_OK;
 }
 
+size_t paged_attention_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_query_tokens,
+                                               const pkv_cache_desc* cache) {
+  if (!cache || cache->num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads ||
+      num_seqs < 0 || num_query_tokens < 0)
+    return 0;
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (group > 16) return 0;
+  return 256 + (prefill_max_items(num_seqs, num_query_tokens, cache->num_kv_heads, group) * 16 + 255) / 256 * 256;
+}
+
+pkv_status paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* query_start, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_query_tokens, int32_t max_context_len,
+                                   float scale, void* out, int32_t out_dtype, void* workspace,
+                                   size_t workspace_bytes, const pkv_cache_desc* cache, void* stream) {
+  if (pkv_status st = check_cache(cache)) return st;
+  if (num_seqs < 0 || num_seqs > (1 << 20)) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", num_seqs);
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d", num_q_heads,
+                cache->num_kv_heads);
+  const int group = num_q_heads / cache->num_kv_heads;
+  if (!tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 128 and query-head groups <= 16");
+  if (cache->num_kv_heads > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d", cache->num_kv_heads);
+  if (num_query_tokens < 0 || max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (num_seqs == 0 || num_query_tokens == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer argument");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+  if (out_dtype != cache->dtype && out_dtype != PKV_F32)
+    return fail(PKV_ERR_UNSUPPORTED, "out dtype %d (must be the cache dtype or f32)", out_dtype);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (static_cast<int64_t>(cache->num_blocks) * cache->num_kv_heads * cache->block_size > (int64_t{1} << 30))
+    return fail(PKV_ERR_UNSUPPORTED, "pool too large for 32-bit row coordinates");
+  const int64_t need_blocks = (static_cast<int64_t>(max_context_len) + cache->block_size - 1) / cache->block_size;
+  if (max_blocks_per_seq < need_blocks)
+    return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d < ceil(max_context_len / block_size)", max_blocks_per_seq);
+  const size_t need = paged_attention_prefill_workspace_bytes(num_seqs, num_q_heads, num_query_tokens, cache);
+  if (!workspace || workspace_bytes < need)
+    return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace ? workspace_bytes : 0);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  int* flag = nullptr;
+  if (pkv_status st = device_flag(&flag)) return st;
+  PrefillParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.out = out;
+  p.work_count = static_cast<int*>(workspace);
+  p.work_list = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);
+  p.err = flag;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = group;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.block_size = cache->block_size;
+  p.num_blocks = cache->num_blocks;
+  p.max_context_len = max_context_len;
+  p.num_query_tokens = num_query_tokens;
+  p.tile_tokens = prefill_tile_tokens(group);
+  p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = launch_prefill_tc(p, cache->dtype, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : cuda_fail(e, "prefill launch");
+}
+
 pkv_status paged_kv_gather(const void* k_cache, const void* v_cache, const int32_t* block_tables,
                            int32_t max_blocks_per_seq, const int32_t* context_lens,
                            int32_t num_seqs, int32_t max_context_len, void* k_out, void* v_out,

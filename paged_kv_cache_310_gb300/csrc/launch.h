@@ -30,6 +30,27 @@ struct DecodeParams {
   float scale_log2;  // softmax scale * log2(e): scores live in the exp2 domain
 };
 
+// Multi-token causal (prefill) attention, tensor cores.
+struct PrefillParams {
+  const void* q;  // [T][Hq][128]
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;  // [S+1]
+  void* out;                   // [T][Hq][128]
+  int4* work_list;
+  int* work_count;
+  int* err;
+  int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
+  int32_t block_size, num_blocks, max_context_len, num_query_tokens, tile_tokens;
+  int32_t out_f32;
+  float scale_log2;
+};
+int prefill_tile_tokens(int group);
+size_t prefill_max_items(int num_seqs, int num_query_tokens, int num_kv_heads, int group);
+cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t stream);
+
 // CUDA-core split-K decode (any supported dtype, head_dim 64/128, group <= 8).
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t stream);
 // Tensor-core (tcgen05) decode: f16/bf16, head_dim 128, group <= 16, persistent CTAs

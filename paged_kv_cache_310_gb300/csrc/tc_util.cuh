@@ -1,0 +1,133 @@
+// tc_util.cuh -- pieces shared by the persistent tensor-core kernels (decode and
+// prefill): the work-list cursor, the role-aware bounded wait, 16-bit packing and
+// output stores, and host helpers for tiled TMA maps of the block pool.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+// Walks this CTA's items: the list is sorted longest first and dealt out in snake
+// order (round k goes left to right when k is even, right to left when odd), which
+// balances the CTAs to within about one chunk.  The next entry is always loaded one
+// item ahead so its latency hides behind the current item.
+struct ItemCursor {
+  const int4* list;
+  int count, k, idx, idx_next;
+  int4 cur, nxt;
+
+  __device__ __forceinline__ int snake(int r) const {
+    return r * static_cast<int>(gridDim.x) +
+           ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                    : static_cast<int>(blockIdx.x));
+  }
+  __device__ __forceinline__ void init(const int4* l, int n) {
+    list = l;
+    count = n;
+    k = 0;
+    idx = snake(0);
+    cur = idx < count ? list[idx] : make_int4(0, 0, 0, 0);
+    idx_next = snake(1);
+    nxt = idx_next < count ? list[idx_next] : make_int4(0, 0, 0, 0);
+  }
+  __device__ __forceinline__ bool valid() const { return idx < count; }
+  __device__ __forceinline__ void advance() {
+    ++k;
+    idx = idx_next;
+    cur = nxt;
+    idx_next = snake(k + 1);
+    if (idx_next < count) nxt = list[idx_next];
+  }
+};
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <typename T>
+__device__ __forceinline__ float round_to(float x) {
+  return Elem<T>::to_float(Elem<T>::from_float(x));
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(void* out, size_t i, float x, int out_f32) {
+  if (out_f32)
+    static_cast<float*>(out)[i] = x;
+  else
+    static_cast<T*>(out)[i] = Elem<T>::from_float(x);
+}
+
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// Pool of rows of 128 16-bit elements seen as 4-D: (64 columns, 8 rows, 2 halves,
+// 8-row groups) with byte strides (-, 256, 128, 2048).  A box of (64, 8, 2, bs/8)
+// is one block's tile for one KV head, landing as [group][half][row][64 columns].
+bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows % 8) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, block_size / 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace
+}  // namespace pkv

@@ -1,0 +1,60 @@
+"""Multi-token causal (prefill / chunked-prefill) attention on the GPU against the
+float64 oracle.  Tolerances as for decode: max-abs <= 2e-3 on fp32 outputs; an output
+in the cache dtype is exactly the RNE rounding of the fp32 output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_310_gb300 as pkv
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # dtype, bs, Hq, Hkv, max_len, min_len, new tokens (None = uniform 1..L)
+    ("bf16", 16, 8, 8, 300, 1, None), ("f16", 16, 32, 4, 700, 100, None), ("bf16", 8, 64, 8, 900, 300, None),
+    ("bf16", 32, 16, 1, 600, 1, None), ("f16", 16, 12, 4, 500, 1, None), ("bf16", 16, 32, 2, 400, 1, None),
+    ("bf16", 16, 8, 2, 2000, 1500, lambda s, L: 128), ("f16", 32, 32, 8, 1200, 1, lambda s, L: (s * 37) % 5),
+    ("bf16", 8, 4, 4, 3000, 2000, lambda s, L: L),
+]
+
+
+def run(w, q, qs, out_dtype=torch.float32):
+    g = w.to("cuda")
+    kc, vc = g.k_cache, g.v_cache
+    out = torch.full(q.shape, float("nan"), dtype=out_dtype, device="cuda")
+    pkv.paged_attention_prefill(q.cuda(), kc, vc, g.block_tables, g.context_lens, qs.cuda(), w.scale, out,
+                                max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    return out
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-bs{c[1]}-{c[2]}x{c[3]}-L{c[4]}" for c in CASES])
+def test_prefill_parity(case):
+    dt, bs, Hq, Hkv, max_len, min_len, nt = case
+    w, q, qs = workloads.prefill_workload(310_900 + CASES.index(case), num_seqs=6, max_len=max_len, min_len=min_len,
+                                          num_q_heads=Hq, num_kv_heads=Hkv, block_size=bs, dtype=dt, new_tokens=nt)
+    if int(qs[-1]) == 0:
+        pytest.skip("no new tokens")
+    ref = oracle.attention_prefill(q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, qs, w.scale)
+    out = run(w, q, qs)
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= 2e-3, f"max-abs {err:.3g}"
+    low = run(w, q, qs, w.dtype)
+    assert torch.equal(low.cpu().view(torch.uint8), out.to(w.dtype).cpu().view(torch.uint8))
+
+
+def test_one_new_token_matches_decode():
+    w, q, qs = workloads.prefill_workload(310_950, num_seqs=9, max_len=1500, min_len=1, num_q_heads=32,
+                                          num_kv_heads=8, new_tokens=lambda s, L: 1)
+    out = run(w, q, qs)
+    g = w.to("cuda")
+    dec = torch.empty_like(out)
+    pkv.paged_attention_decode(q.cuda(), g.k_cache, g.v_cache, g.block_tables, g.context_lens, w.scale, dec,
+                               max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert (out - dec).abs().max().item() <= 2e-3

@@ -292,3 +292,35 @@ def random_workload(seed, *, num_seqs, max_len, num_q_heads, num_kv_heads, head_
                              num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                              block_size=block_size, ctx=ctx, block_keys=keys, owned_rows=owned,
                              cow=[], num_blocks=unique + extra_blocks, canary=canary, gen=g)
+
+
+def prefill_workload(seed, *, num_seqs, max_len, num_q_heads, num_kv_heads, head_dim=128, block_size=16,
+                     dtype="bf16", min_len=1, new_tokens=None, canary=True, pool_device="cpu"):
+    """A pool whose every context row is valid, plus new tokens for multi-token attention.
+
+    Context lengths are uniform in [min_len, max_len]; sequence s brings
+    new_tokens(s, L) new tokens (default: uniform in [1, L]), the last ones of its
+    context.  Returns (workload, q [T, Hq, D], query_start int32 [S+1]).
+    """
+    g = torch.Generator().manual_seed(seed)
+    tdtype = DTYPES[dtype]
+    ctx = torch.randint(min_len, max_len + 1, (num_seqs,), generator=g).tolist()
+    keys, _ = private_layout(ctx, block_size)
+    owned = {}
+    for s, n in enumerate(ctx):
+        for i, k in enumerate(keys[s]):
+            owned[k] = [r for r in range(block_size) if i * block_size + r < n]
+    unique = sum(len(k) for k in keys)
+    w = build_from_layout(name=f"prefill seed {seed}", seed=seed, dtype=dtype, num_q_heads=num_q_heads,
+                          num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size, ctx=ctx,
+                          block_keys=keys, owned_rows=owned, cow=[], num_blocks=unique + 3, canary=canary,
+                          gen=g, pool_device=pool_device)
+    if new_tokens is None:
+        nq = [int(torch.randint(0, n, (1,), generator=g)) + 1 if n else 0 for n in ctx]
+    else:
+        nq = [min(n, int(new_tokens(s, n))) for s, n in enumerate(ctx)]
+    qs = [0]
+    for n in nq:
+        qs.append(qs[-1] + n)
+    q = _randn((qs[-1], num_q_heads, head_dim), g, tdtype)
+    return w, q, torch.tensor(qs, dtype=torch.int32)
