@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true", help="measure causal multi-token (prefill) attention instead")
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size (8/16/32)")
     ap.add_argument("--identity-tables", action="store_true",
                     help="physical blocks in logical order (contiguous sequences): the indirection A/B")
@@ -211,10 +212,84 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args):
+    """--prefill: causal multi-token attention (chunked prefill) on tensor cores.
+
+    Workload: 32 sequences with contexts uniform in [1024, 4096], each bringing its last
+    512 tokens as new queries, 64 query / 8 KV heads, head_dim 128, bf16, block size 16.
+    Algorithmic flops: 4 * Hq * D * (p + 1) per new token at position p (QK and PV,
+    causal); the kernel's hi/lo probability split doubles the PV MMAs, which is not
+    counted.
+    """
+    import paged_kv_cache_310_gb300 as pkv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    nq = 512
+    w, q, qs = workloads.prefill_workload(310_990, num_seqs=32, max_len=4096, min_len=1024, num_q_heads=64,
+                                          num_kv_heads=8, block_size=16, dtype="bf16",
+                                          new_tokens=lambda s, L: nq, canary=False, pool_device=dev)
+    g = w.to(dev)
+    qd, qsd = q.to(dev), qs.to(dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.paged_attention_prefill(qd, g.k_cache, g.v_cache, g.block_tables, g.context_lens, qsd, w.scale, out,
+                                    max_context_len=w.max_context_len)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pkv.device_error() != 0:
+        raise SystemExit("device error flag set during warm-up")
+    clocks = ClockSampler(dev.index or 0)
+    time.sleep(0.3)
+    steps = min(args.steps, 500)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    lens = w.context_lens.tolist()
+    Hq, D = w.num_q_heads, w.head_dim
+    flops = sum(4 * Hq * D * (L - nq + i + 1) for L in lens for i in range(nq))
+    kv = sum(lens) * 2 * w.num_kv_heads * D * 2
+    qo = 2 * int(qs[-1]) * Hq * D * 2
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak, tkind = float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        tpeak, tkind = 1900.0, "fallback"
+    hpeak, hkind = peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    line = {"metric": "paged prefill attention (causal): TFLOP/s, new tokens/s", "value": tflops, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "chunked prefill: 32 seqs, contexts U[1024,4096], last 512 tokens new, "
+                                   "64/8 heads, D128, bf16, bs16", "new_tokens": int(qs[-1])},
+            "tokens_per_s": int(qs[-1]) / (ms * 1e-3),
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+                         "frac": tflops / tpeak, "peak_source": tkind, "traffic": None,
+                         "kernel": "paged_attention_prefill (work list + prefill_tc)",
+                         "algorithmic_flops_per_launch": flops},
+            "hbm": {"algorithmic_bytes_per_launch": kv + qo, "achieved_gbs": (kv + qo) / (ms * 1e-3) / 1e9,
+                    "peak": hpeak, "peak_source": hkind},
+            "gpu_launches": 2 * steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
