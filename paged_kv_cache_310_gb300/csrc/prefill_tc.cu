@@ -399,26 +399,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // pass 2: probabilities as hi + lo parts into P^T's swizzled rows
         float rowsum = 0.f;
         unsigned char* ph = smem + kOffP + sb * kPBytes;
+        const bool diagonal = kbase + kKC - 1 > qpos;  // only then does the mask cut this row
+        const float neg_m = -m;
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
           float sv[16];
           tmem_load16(lane_base + sb * 64 + q * 16, sv);
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            float hi[8], lo[8];
+            uint32_t hw[4], lw[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 8; i += 2) {
               const int jj = q * 16 + half * 8 + i;
-              const float pe = kbase + jj <= qpos ? exp2f(sv[half * 8 + i] * p.scale_log2 - m) : 0.f;
-              rowsum += pe;
-              hi[i] = round_to<T>(pe);
-              lo[i] = round_to<T>(pe - hi[i]);
+              float p0 = exp2_approx(fmaf(sv[half * 8 + i], p.scale_log2, neg_m));
+              float p1 = exp2_approx(fmaf(sv[half * 8 + i + 1], p.scale_log2, neg_m));
+              if (diagonal) {
+                p0 = kbase + jj <= qpos ? p0 : 0.f;
+                p1 = kbase + jj + 1 <= qpos ? p1 : 0.f;
+              }
+              rowsum += p0 + p1;
+              float h0, h1;
+              hw[i / 2] = pack2_split<T>(p0, p1, h0, h1);  // rounded pair, and its values
+              lw[i / 2] = pack2<T>(p0 - h0, p1 - h1);      // exact remainders, rounded
             }
             const int off = swz_keys(t, q * 2 + half);
-            *reinterpret_cast<uint4*>(ph + off) = make_uint4(pack2<T>(hi[0], hi[1]), pack2<T>(hi[2], hi[3]),
-                                                             pack2<T>(hi[4], hi[5]), pack2<T>(hi[6], hi[7]));
-            *reinterpret_cast<uint4*>(ph + kPPart + off) = make_uint4(
-                pack2<T>(lo[0], lo[1]), pack2<T>(lo[2], lo[3]), pack2<T>(lo[4], lo[5]), pack2<T>(lo[6], lo[7]));
+            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(ph + kPPart + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         l += rowsum;

@@ -74,6 +74,33 @@ __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// Round a pair to the 16-bit type (RNE) and also return the rounded values as floats.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2_split(float a, float b, float& ra, float& rb);
+template <>
+__device__ __forceinline__ uint32_t pack2_split<__nv_bfloat16>(float a, float b, float& ra, float& rb) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  const uint32_t u = *reinterpret_cast<uint32_t*>(&v);
+  ra = __uint_as_float(u << 16);
+  rb = __uint_as_float(u & 0xffff0000u);
+  return u;
+}
+template <>
+__device__ __forceinline__ uint32_t pack2_split<__half>(float a, float b, float& ra, float& rb) {
+  __half2 v = __floats2half2_rn(a, b);
+  const float2 f = __half22float2(v);
+  ra = f.x;
+  rb = f.y;
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; exp2(-inf) = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T>
 __device__ __forceinline__ float round_to(float x) {
   return Elem<T>::to_float(Elem<T>::from_float(x));
