@@ -371,15 +371,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         tc_fence_after();
         const int kbase = k * kKC;
+        const bool diagonal = kbase + kKC - 1 > qpos;  // only then does the mask cut this row
         // pass 1: the row's chunk max under the causal mask (16-column pieces of S)
         float cm = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
           float sv[16];
           tmem_load16(lane_base + sb * 64 + q * 16, sv);
+          if (diagonal) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (kbase + q * 16 + i <= qpos) cm = fmaxf(cm, sv[i] * p.scale_log2);
+            for (int i = 0; i < 16; ++i)
+              if (kbase + q * 16 + i <= qpos) cm = fmaxf(cm, sv[i] * p.scale_log2);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cm = fmaxf(cm, sv[i] * p.scale_log2);
+          }
         }
         // lazy rescale: keep m unless the chunk brings a score more than the slack above
         float alpha = 1.f;
@@ -399,7 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // pass 2: probabilities as hi + lo parts into P^T's swizzled rows
         float rowsum = 0.f;
         unsigned char* ph = smem + kOffP + sb * kPBytes;
-        const bool diagonal = kbase + kKC - 1 > qpos;  // only then does the mask cut this row
         const float neg_m = -m;
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
