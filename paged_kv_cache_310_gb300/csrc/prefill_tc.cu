@@ -9,28 +9,33 @@
 // p = context_lens[s] - n_s + i and attends to positions 0..p through the block table.
 // One new token per sequence is exactly paged decode.
 //
-// Work item = (sequence, KV head, query tile).  A tile is 128 query rows: TQ =
-// floor(128 / G) consecutive new tokens times the G query heads of the KV head, row
-// r = token * G + head (rows past TQ * G are padding).  Per 64-key chunk:
+// A tile is 128 query rows: TQ = floor(128 / G) consecutive new tokens times the G
+// query heads of one KV head, row r = token * G + head (rows past TQ * G are padding).
+// A work item is a PAIR of consecutive tiles of one (sequence, KV head): both tiles
+// consume the same K/V chunks, so each chunk is read once for 256 query rows.  Per
+// 64-key chunk and tile:
 //   S[128 rows x 64 keys] = Q . K^T            (M=128, N=64,  K=128 dims)
-//   O[128 rows x 128 dims] = P . V             (M=128, N=128, K=64 keys), twice:
+//   O[128 rows x 128 dims] += P . V            (M=128, N=128, K=64 keys), twice:
 // the probabilities as hi = round(p) and lo = round(p - hi) in the cache dtype, so
 // the 16-bit operand costs about 2^-17 relative per weight.  S (double-buffered) and
-// O live in TMEM; the MMA accumulates O over the tile's chunks.  Softmax is row-local
-// (no cross-thread reduction) with a lazy rescale: a row keeps the maximum it used
-// for its probabilities until a chunk brings a score more than 8 (log2 units) above
-// it -- probabilities stay <= 256 -- and only then is its O row rescaled in TMEM.
-// O is double-buffered by tile and read out once, at the tile's end.
+// O of each tile live in TMEM; the MMA accumulates O over the item's chunks.  Softmax
+// is row-local (no cross-thread reduction) with a lazy rescale: a row keeps the
+// maximum it used for its probabilities until a chunk brings a score more than 8
+// (log2 units) above it -- probabilities stay <= 256 -- and only then is its O row
+// rescaled in TMEM.
 //
-// Roles (192 threads, persistent CTAs over a longest-first work list dealt in snake
+// Roles (320 threads, persistent CTAs over a longest-first work list dealt in snake
 // order):
-//  * warp 4, producer: loads the tile's 128 query rows (plain loads, written in the
+//  * warps 0-3 and 4-7: one softmax warpgroup per tile of the pair (thread = query
+//    row = TMEM lane); while one group computes probabilities the tensor cores work
+//    for the other.
+//  * warp 8, producer: loads both tiles' query rows (plain loads, written in the
 //    128-byte swizzled operand layout), then per chunk one 4-D TMA box per block for
-//    K and one for V into a 3-stage ring (blocks past the tile's last position are
+//    K and one for V into a 3-stage ring (blocks past the pair's last position are
 //    loaded from outside the tensor: zero fill).
-//  * warp 5, MMA: one lane polls and issues QK(c) once K/V and Q are in and an S
-//    buffer is free, PV(c) once P(c) (and any rescale of O) is written.
-//  * warps 0-3: thread t owns query row t.
+//  * warp 9, MMA: one lane polls four streams -- QK and PV of each tile -- and issues
+//    whatever is ready; a ring stage is released once both tiles' PVs of its chunk
+//    are issued (their commit fires when they complete).
 #include <climits>
 #include <type_traits>
 
@@ -42,29 +47,38 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kGroups = 2;                 // tiles per item, one softmax warpgroup each
+constexpr int kThreads = (4 * kGroups + 2) * 32;
+constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = 4 * kGroups + 1;
 constexpr int kRows = 128;                 // query rows per tile (M)
 constexpr int kKC = 64;                    // keys per chunk
 constexpr int kStages = 3;
 constexpr int kGroup = 2048;               // 8-row group of a 128-dim tile: two 64-column halves
 constexpr int kKVTile = kKC * 256;         // K (or V) of one chunk: 16 KB
 constexpr int kStageBytes = 2 * kKVTile;   // K then V
-constexpr int kQBytes = kRows * 256;       // 32 KB: [16 groups][2 halves][8 rows][128 B]
+constexpr int kQBytes = kRows * 256;       // 32 KB per tile: [16 groups][2 halves][8 rows][128 B]
 constexpr int kPPart = kRows * kKC * 2;    // 16 KB: [16 groups][8 rows][128 B], one part
-constexpr int kPBytes = 2 * kPPart;        // hi part then lo part
+constexpr int kPBytes = 2 * kPPart;        // per tile: hi part then lo part
 constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 2 * kStages + 7 * 2 + 1;
+constexpr int kOffP = kOffQ + kGroups * kQBytes;
+constexpr int kOffBar = kOffP + kGroups * kPBytes;
+// ring full/empty, qfull, qempty, then per tile: sfull[2], sfree[2], pfull, pvdone[2]; drain
+constexpr int kNumBars = 2 * kStages + 2 + kGroups * 7 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64;
-constexpr uint32_t kTmemCols = 512;        // S[2] at 0/64 (64 columns), O[2] at 128/256 (128 columns)
+constexpr uint32_t kTmemCols = 512;        // per tile g: S[2] at 256g + 0/64, O at 256g + 128
 constexpr float kRescaleSlack = 8.f;       // log2 units a row's max may grow before O is rescaled
 constexpr int kListThreads = 1024;
 constexpr int kMaxBuckets = 1024;          // chunk-count buckets of the work list (last one open-ended)
 
 struct Bars {
-  uint64_t *full, *empty, *qfull, *qempty, *sfull, *sfree, *pfull, *ofull, *ofree, *drain;
+  uint64_t *full, *empty, *qfull, *qempty, *drain, *grp;
+  // per tile g: sfull[2], sfree[2], pfull, pvdone[2] (addresses computed, so a
+  // runtime tile index needs no local-memory table)
+  __device__ __forceinline__ uint64_t* sfull(int g, int i) const { return grp + 7 * g + i; }
+  __device__ __forceinline__ uint64_t* sfree(int g, int i) const { return grp + 7 * g + 2 + i; }
+  __device__ __forceinline__ uint64_t* pfull(int g) const { return grp + 7 * g + 4; }
+  __device__ __forceinline__ uint64_t* pvdone(int g, int i) const { return grp + 7 * g + 5 + i; }
 };
 
 __device__ __forceinline__ Bars carve(unsigned char* smem) {
@@ -73,13 +87,9 @@ __device__ __forceinline__ Bars carve(unsigned char* smem) {
   r.full = b;
   r.empty = b + kStages;
   r.qfull = b + 2 * kStages;
-  r.qempty = r.qfull + 2;
-  r.sfull = r.qempty + 2;
-  r.sfree = r.sfull + 2;
-  r.pfull = r.sfree + 2;
-  r.ofull = r.pfull + 2;
-  r.ofree = r.ofull + 2;
-  r.drain = r.ofree + 2;
+  r.qempty = r.qfull + 1;
+  r.grp = r.qempty + 1;
+  r.drain = r.grp + 7 * kGroups;
   return r;
 }
 
@@ -89,19 +99,22 @@ struct PrefillArgs {
   PrefillParams p;
 };
 
-// {s, g | ntile << 16, first query row, position of the tile's first token}
-struct Tile {
-  int s, g, ntile, qrow0, pos0, nchunks;
+// {s, g | ntile_a << 12 | ntile_b << 20, first query row of tile a, position of its first token}
+struct Item {
+  int s, g, na, nb, qrow0, pos0, last, nchunks;  // na, nb: tokens in tile a, tile b
+  __device__ __forceinline__ int ntok(int tile) const { return tile ? nb : na; }
 };
 
-__device__ __forceinline__ Tile unpack_tile(int4 e) {
-  Tile t;
+__device__ __forceinline__ Item unpack_item(int4 e, int tq) {
+  Item t;
   t.s = e.x;
-  t.g = e.y & 0xffff;
-  t.ntile = static_cast<int>(static_cast<unsigned>(e.y) >> 16);
+  t.g = e.y & 0xfff;
+  t.na = (e.y >> 12) & 0xff;
+  t.nb = (static_cast<unsigned>(e.y) >> 20) & 0xff;
   t.qrow0 = e.z;
   t.pos0 = e.w;
-  t.nchunks = (t.pos0 + t.ntile + kKC - 1) / kKC;
+  t.last = t.pos0 + (t.nb ? tq + t.nb : t.na) - 1;  // position of the pair's last token
+  t.nchunks = (t.last + kKC) / kKC;
   return t;
 }
 
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);
   int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);
-  const int G = p.group;
+  const int G = p.group, TQ = p.tile_tokens;
   const int num_items = *p.work_count;
 
   if (threadIdx.x == 0) {
@@ -133,27 +146,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&bars.full[i], 1);
       mbar_init(&bars.empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.qfull[i], 1);
-      mbar_init(&bars.qempty[i], 1);
-      mbar_init(&bars.sfull[i], 1);
-      mbar_init(&bars.sfree[i], 4);
-      mbar_init(&bars.pfull[i], 4);
-      mbar_init(&bars.ofull[i], 1);
-      mbar_init(&bars.ofree[i], 4);
+    mbar_init(bars.qfull, 1);
+    mbar_init(bars.qempty, 1);
+    for (int g = 0; g < kGroups; ++g) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(bars.sfull(g, i), 1);
+        mbar_init(bars.sfree(g, i), 4);
+        mbar_init(bars.pvdone(g, i), 1);
+      }
+      mbar_init(bars.pfull(g), 4);
     }
     *abort_flag = 0;
     *issued_slot = 0;
     *waited_slot = 0;
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ============================ producer ============================
     if (lane == 0) {
       prefetch_tensormap(&a.tk);
@@ -166,37 +180,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     int c = 0, j = 0;
     bool ok = true;
     ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
-      const Tile it = unpack_tile(cur.cur);
-      const int qb = j & 1;
-      // ---- the tile's query rows, swizzled, zero past the tile ----
-      ok = j < 2 || __shfl_sync(0xffffffffu, lane == 0 ? wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1,
-                                                                   abort_flag, p.err)
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance(), ++j) {
+      const Item it = unpack_item(cur.cur, TQ);
+      // ---- both tiles' query rows, swizzled, zero past each tile; the previous
+      //      item's QKs must be done with the buffers ----
+      ok = j < 1 || __shfl_sync(0xffffffffu, lane == 0 ? wait_role(bars.qempty, (j - 1) & 1, abort_flag, p.err)
                                                        : true, 0);
       if (!ok) break;
-      unsigned char* qbuf = smem + kOffQ + qb * kQBytes;
-      const int valid_rows = it.ntile * G;
 #pragma unroll 1
-      for (int r = lane; r < kRows; r += 32) {
-        const bool valid = r < valid_rows;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-            (static_cast<size_t>(it.qrow0 + r / G) * p.num_q_heads + it.g * G + r % G) * 128);
+      for (int g = 0; g < kGroups; ++g) {
+        unsigned char* qbuf = smem + kOffQ + g * kQBytes;
+        const int valid_rows = it.ntok(g) * G;
+#pragma unroll 1
+        for (int r = lane; r < kRows; r += 32) {
+          const bool valid = r < valid_rows;
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+              (static_cast<size_t>(it.qrow0 + g * TQ + r / G) * p.num_q_heads + it.g * G + r % G) * 128);
 #pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {
-          const uint4 v = valid ? src[c16] : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(qbuf + swz_dims(r, c16)) = v;
+          for (int c16 = 0; c16 < 16; ++c16) {
+            const uint4 v = valid ? src[c16] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(qbuf + swz_dims(r, c16)) = v;
+          }
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.qfull[qb]);
+      if (lane == 0) mbar_arrive(bars.qfull);
       // ---- K/V chunks ----
-      const int pos_last = it.pos0 + it.ntile - 1;
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
         const int st = c % kStages;
         const int lb = k * blocks_per_chunk + lane;  // logical block of this lane
-        const bool live = lane < blocks_per_chunk && lb * bs <= pos_last;
+        const bool live = lane < blocks_per_chunk && lb * bs <= it.last;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
           ok = c < kStages || wait_role(&bars.empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
@@ -220,9 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         if (lane == 0) *issued_slot = c + 1;
       }
-      ++j;
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ============================
     if (lane == 0) {
       constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -231,71 +245,93 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const uint32_t ring = smem_addr(smem);
       const uint32_t qbase = smem_addr(smem + kOffQ);
       const uint32_t pbase = smem_addr(smem + kOffP);
-      ItemCursor qcur;
-      qcur.init(p.work_list, num_items);
-      int qk = 0, qj = 0;
-      int qn = qcur.valid() ? unpack_tile(qcur.cur).nchunks : 0;
-      // PV cursor: tile index (selects the O buffer), chunk within the tile
-      ItemCursor pcur;
-      pcur.init(p.work_list, num_items);
-      int pk = 0, pj = 0;
-      int pn = pcur.valid() ? unpack_tile(pcur.cur).nchunks : 0;
-      int qc = 0, pc = 0;
+      // one cursor per stream: QK and PV of each tile walk the same chunk sequence
+      struct Stream {
+        ItemCursor cur;
+        int k, n, c;  // chunk within the item, chunks in the item, global chunk
+      };
+      Stream qs[kGroups], ps[kGroups];
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        qs[g].cur.init(p.work_list, num_items);
+        ps[g].cur.init(p.work_list, num_items);
+        qs[g].k = ps[g].k = 0;
+        qs[g].c = ps[g].c = 0;
+        qs[g].n = ps[g].n = qs[g].cur.valid() ? unpack_item(qs[g].cur.cur, TQ).nchunks : 0;
+      }
+      auto step = [&](Stream& s) {
+        ++s.c;
+        if (++s.k == s.n) {
+          s.k = 0;
+          s.cur.advance();
+          s.n = s.cur.valid() ? unpack_item(s.cur.cur, TQ).nchunks : 0;
+        }
+      };
+      int q_items = 0;     // items whose query buffers both tiles are done with
+      int q_last = 0;      // tiles that issued the current item's last QK
       uint64_t idle_since = global_timer_ns();
-      while (qcur.valid() || pc < qc) {
-        bool progressed = false;
-        if (qcur.valid()) {
-          const int st = qc % kStages, sb = qc & 1, qb = qj & 1;
-          if ((qk > 0 || mbar_try_wait(&bars.qfull[qb], (qj >> 1) & 1)) &&
-              mbar_try_wait(&bars.full[st], (qc / kStages) & 1) &&
-              (qc < 2 || mbar_try_wait(&bars.sfree[sb], ((qc >> 1) - 1) & 1))) {
-            *waited_slot = qc + 1;
+      while (true) {
+        bool active = false, progressed = false;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          Stream& s = qs[g];
+          if (!s.cur.valid()) continue;
+          active = true;
+          if (s.cur.k != q_items) continue;  // one query buffer per tile: no running ahead
+          const int c = s.c, st = c % kStages, sb = c & 1;
+          if ((s.k > 0 || mbar_try_wait(bars.qfull, q_items & 1)) &&
+              mbar_try_wait(&bars.full[st], (c / kStages) & 1) &&
+              (c < 2 || mbar_try_wait(bars.sfree(g, sb), ((c >> 1) - 1) & 1))) {
+            if (g == 0) *waited_slot = c + 1;
             tc_fence_after();
             const uint32_t kb = ring + st * kStageBytes;
-            const uint32_t qa = qbase + qb * kQBytes;
+            const uint32_t qa = qbase + g * kQBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 32;
-              mma_f16(tmem + sb * 64, smem_desc(qa + off, 16, kGroup, kLayoutSwizzle128),
+              mma_f16(tmem + g * 256 + sb * 64, smem_desc(qa + off, 16, kGroup, kLayoutSwizzle128),
                       smem_desc(kb + off, 16, kGroup, kLayoutSwizzle128), idesc_qk, kk > 0);
             }
-            mma_commit(&bars.sfull[sb]);
-            ++qc;
-            if (++qk == qn) {  // the tile's last QK: its query buffer can be refilled
-              mma_commit(&bars.qempty[qb]);
-              qk = 0;
-              ++qj;
-              qcur.advance();
-              qn = qcur.valid() ? unpack_tile(qcur.cur).nchunks : 0;
+            mma_commit(bars.sfull(g, sb));
+            if (s.k == s.n - 1 && ++q_last == kGroups) {  // both tiles' queries consumed
+              mma_commit(bars.qempty);
+              q_last = 0;
+              ++q_items;
             }
+            step(s);
             progressed = true;
           }
         }
-        if (pc < qc) {
-          const int pb = pc & 1, st = pc % kStages;
-          if (mbar_try_wait(&bars.pfull[pb], (pc >> 1) & 1)) {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          Stream& s = ps[g];
+          if (!s.cur.valid()) continue;
+          active = true;
+          if (s.c >= qs[g].c) continue;  // its QK comes first
+          const int c = s.c, st = c % kStages;
+          if (mbar_try_wait(bars.pfull(g), c & 1)) {
             tc_fence_after();
             const uint32_t vbase = ring + st * kStageBytes + kKVTile;
-            const uint32_t pa = pbase + pb * kPBytes;
-            const uint32_t od = tmem + 128 + (pj & 1) * 128;  // this tile's O buffer
+            const uint32_t pa = pbase + g * kPBytes;
+            const uint32_t od = tmem + g * 256 + 128;
 #pragma unroll
             for (int kk = 0; kk < kKC / 16; ++kk) {
               const uint64_t bd = smem_desc(vbase + kk * 2 * kGroup, 1024, kGroup, kLayoutSwizzle128);
-              mma_f16(od, smem_desc(pa + kk * 32, 16, 1024, kLayoutSwizzle128), bd, idesc_pv, pk > 0 || kk > 0);
+              mma_f16(od, smem_desc(pa + kk * 32, 16, 1024, kLayoutSwizzle128), bd, idesc_pv, s.k > 0 || kk > 0);
               mma_f16(od, smem_desc(pa + kPPart + kk * 32, 16, 1024, kLayoutSwizzle128), bd, idesc_pv, true);
             }
-            mma_commit(&bars.ofull[pb]);
-            mma_commit(&bars.empty[st]);
-            ++pc;
-            if (++pk == pn) {
-              pk = 0;
-              ++pj;
-              pcur.advance();
-              pn = pcur.valid() ? unpack_tile(pcur.cur).nchunks : 0;
-            }
+            mma_commit(bars.pvdone(g, c & 1));
+            // the stage is free once every tile's PV of this chunk has completed
+            bool all = true;
+#pragma unroll
+            for (int h = 0; h < kGroups; ++h)
+              if (h != g && ps[h].c <= c) all = false;
+            if (all) mma_commit(&bars.empty[st]);
+            step(s);
             progressed = true;
           }
         }
+        if (!active) break;
         if (progressed) {
           idle_since = global_timer_ns();
         } else {
@@ -310,28 +346,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     __syncwarp();
   } else {
-    // ============================ softmax warps ============================
-    const int t = threadIdx.x;  // query row of the tile = TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    int c = 0, j = 0;
+    // ============================ softmax warpgroups ============================
+    const int grp = warp / 4;                 // which tile of the pair
+    const int t = threadIdx.x % 128;          // query row of the tile = TMEM lane
+    const int wq = warp % 4;                  // lane quarter
+    const uint32_t lane_base = tmem + grp * 256 + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t obuf = lane_base + 128;
+    int c = 0;
     bool ok = true;
-    // the previous tile, read out once this tile's first chunk is under way
     int prev_row = -1, prev_c = -1;
     float prev_l = 1.f;
 
-    // Warp-uniform: has PV of chunk cc completed?  Waited in chunk order per barrier.
+    // Warp-uniform: has this tile's PV of chunk cc completed?  (waited in chunk order)
     auto pv_done = [&](int cc) -> bool {
-      return __all_sync(0xffffffffu, wait_role(&bars.ofull[cc & 1], (cc >> 1) & 1, abort_flag, p.err));
+      return __all_sync(0xffffffffu, wait_role(bars.pvdone(grp, cc & 1), (cc >> 1) & 1, abort_flag, p.err));
     };
-    // The finished tile's output rows: O / l, once the tile's last PV has completed.
-    auto finish = [&](int row, int last_c, float lsum, int buf) -> bool {
-      if (!pv_done(last_c)) return false;
+    // A finished item's output rows: O / l (O is final: its last PV was waited for).
+    auto finish = [&](int row, float lsum) {
       tc_fence_after();
       const float inv = 1.f / lsum;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float o[16];
-        tmem_load16(lane_base + 128 + buf * 128 + q * 16, o);
+        tmem_load16(obuf + q * 16, o);
         if (row >= 0) {
           if (p.out_f32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(row) * 128 + q * 16);
@@ -350,22 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
       }
       tc_fence_before();
-      return true;
     };
 
     ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance(), ++j) {
-      const Tile it = unpack_tile(cur.cur);
-      const int valid_rows = it.ntile * G;
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+      const Item it = unpack_item(cur.cur, TQ);
+      const int valid_rows = it.ntok(grp) * G;
       const bool row_valid = t < valid_rows;
-      const int pos_last = it.pos0 + it.ntile - 1;
-      const int qpos = row_valid ? it.pos0 + t / G : pos_last;  // padding rows act as the last token
-      const int out_row = row_valid ? (it.qrow0 + t / G) * p.num_q_heads + it.g * G + t % G : -1;
-      const uint32_t obuf = tmem + 128 + (j & 1) * 128;
+      const int qpos = row_valid ? it.pos0 + grp * TQ + t / G : it.last;  // padding rows act as the last token
+      const int out_row = row_valid ? (it.qrow0 + grp * TQ + t / G) * p.num_q_heads + it.g * G + t % G : -1;
       float m = 0.f, l = 0.f;  // max used for this row's probabilities, running row sum
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
-        if (!__all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, wait_role(bars.sfull(grp, sb), (c >> 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -388,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
         // lazy rescale: keep m unless the chunk brings a score more than the slack above
+        // (a chunk entirely past this row's position gives cm = -inf and changes nothing)
         float alpha = 1.f;
         if (k == 0) {
           m = cm;  // key 0 is never masked: finite
@@ -396,15 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           m = cm;
           l *= alpha;
         }
-        const bool rescale = k > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-        // P(c) reuses the buffer P(c-2) filled: that PV must be done
-        if (c >= 2 && !pv_done(c - 2)) {
+        // the previous chunk's PV (reads P, accumulates O) must be done before P is
+        // rewritten, O rescaled, or -- at an item's first chunk -- O read out
+        if (c >= 1 && !pv_done(c - 1)) {
           ok = false;
           break;
         }
-        // pass 2: probabilities as hi + lo parts into P^T's swizzled rows
+        if (k == 0 && prev_c >= 0) {
+          finish(prev_row, prev_l);
+          prev_c = -1;
+        }
+        if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int q = 0; q < 8; ++q) {
+            float o[16];
+            tmem_load16(obuf + q * 16, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tmem_store16(obuf + q * 16, o);
+          }
+          tc_fence_before();
+        }
+        // pass 2: probabilities as hi + lo parts into P's swizzled rows
         float rowsum = 0.f;
-        unsigned char* ph = smem + kOffP + sb * kPBytes;
+        unsigned char* ph = smem + kOffP + grp * kPBytes;
         const float neg_m = -m;
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
@@ -435,27 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         l += rowsum;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.sfree[sb]);
-        // a row whose max jumped: rescale its O row in TMEM once PV(c-1) is done
-        if (rescale) {
-          if (!pv_done(c - 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int q = 0; q < 8; ++q) {
-            float o[16];
-            tmem_load16(obuf + (static_cast<uint32_t>(warp * 32) << 16) + q * 16, o);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tmem_store16(obuf + (static_cast<uint32_t>(warp * 32) << 16) + q * 16, o);
-          }
-          tc_fence_before();
-        }
-        // V rows past the tile's last position inside loaded blocks: zero them (a NaN
-        // there would survive a zero weight)
-        const int rows_needed = pos_last + 1 - kbase;
+        if (lane == 0) mbar_arrive(bars.sfree(grp, sb));
+        // V rows past the pair's last position inside loaded blocks: zero them (a NaN
+        // there would survive a zero weight).  Both groups write the same zeros.
+        const int rows_needed = it.last + 1 - kbase;
         if (t < kKC && rows_needed < kKC) {
           const int rows_loaded = min(kKC, (rows_needed + p.block_size - 1) / p.block_size * p.block_size);
           if (t >= rows_needed && t < rows_loaded) {
@@ -469,33 +503,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.pfull[sb]);
-        // the previous tile's O can be read now that this tile's first chunk is queued
-        if (k == 0 && prev_c >= 0) {
-          if (!finish(prev_row, prev_c, prev_l, (j - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          prev_c = -1;
-        }
+        if (lane == 0) mbar_arrive(bars.pfull(grp));
       }
       if (!ok) break;
       prev_row = out_row;
       prev_c = c - 1;
       prev_l = l;
     }
-    if (ok && prev_c >= 0) finish(prev_row, prev_c, prev_l, (j - 1) & 1);
+    if (ok && prev_c >= 0 && pv_done(prev_c)) finish(prev_row, prev_l);
     __syncwarp();
   }
 
   // ---------------- teardown ----------------
   __syncthreads();
   if (*abort_flag) {
-    if (warp == 4 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
       for (int c = *waited_slot; c < *issued_slot; ++c)
         if (!mbar_wait(&bars.full[c % kStages], (c / kStages) & 1)) break;
     }
-    if (warp == 5 && lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
       mbar_init(bars.drain, 1);
       fence_barrier_init();
       mma_commit(bars.drain);
@@ -505,15 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Work list: one entry per (sequence, KV head, query tile), sorted by chunk count,
-// longest first (counting sort; order inside one count does not matter).
+// Work list: one entry per (sequence, KV head, pair of query tiles), sorted by chunk
+// count, longest first (counting sort; order inside one count does not matter).
 __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid_constant__ PrefillParams p) {
   __shared__ int hist[kMaxBuckets];
   __shared__ int next[kMaxBuckets];
-  const int H = p.num_kv_heads, TQ = p.tile_tokens;
+  const int H = p.num_kv_heads, TQ = p.tile_tokens, span = kGroups * TQ;
   for (int i = threadIdx.x; i < kMaxBuckets; i += kListThreads) hist[i] = 0;
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
@@ -522,9 +548,8 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
       set_error(p.err, kErrLength);
       continue;
     }
-    for (int t0 = 0; t0 < n; t0 += TQ) {
-      const int ntile = min(TQ, n - t0), pos0 = L - n + t0;
-      const int nch = (pos0 + ntile + kKC - 1) / kKC;
+    for (int t0 = 0; t0 < n; t0 += span) {
+      const int nch = (L - n + t0 + min(span, n - t0) + kKC - 1) / kKC;
       atomicAdd(&hist[min(nch, kMaxBuckets - 1)], H);
     }
   }
@@ -541,12 +566,12 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
   for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
     const int n = p.query_start[s + 1] - p.query_start[s], L = p.context_lens[s];
     if (n < 0 || L < n || L > p.max_context_len) continue;
-    for (int t0 = 0; t0 < n; t0 += TQ) {
-      const int ntile = min(TQ, n - t0), pos0 = L - n + t0;
-      const int nch = (pos0 + ntile + kKC - 1) / kKC;
+    for (int t0 = 0; t0 < n; t0 += span) {
+      const int na = min(TQ, n - t0), nb = max(0, min(TQ, n - t0 - TQ));
+      const int nch = (L - n + t0 + na + nb + kKC - 1) / kKC;
       const int pos = atomicAdd(&next[min(nch, kMaxBuckets - 1)], H);
       for (int g = 0; g < H; ++g)
-        p.work_list[pos + g] = make_int4(s, g | (ntile << 16), p.query_start[s] + t0, pos0);
+        p.work_list[pos + g] = make_int4(s, g | (na << 12) | (nb << 20), p.query_start[s] + t0, L - n + t0);
     }
   }
 }
@@ -569,11 +594,12 @@ cudaError_t launch_prefill_t(const PrefillArgs& args, int grid, cudaStream_t str
 int prefill_tile_tokens(int group) { return kRows / group; }
 
 size_t prefill_max_items(int num_seqs, int num_query_tokens, int num_kv_heads, int group) {
-  const int TQ = kRows / group;
-  return (static_cast<size_t>(num_query_tokens) / TQ + num_seqs) * num_kv_heads;
+  const int span = kGroups * (kRows / group);
+  return (static_cast<size_t>(num_query_tokens) / span + num_seqs) * num_kv_heads;
 }
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t stream) {
+  if (p.num_kv_heads > 4095) return cudaErrorInvalidValue;  // packed into 12 bits of a list entry
   PrefillArgs args;
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
