@@ -9,33 +9,36 @@
 // p = context_lens[s] - n_s + i and attends to positions 0..p through the block table.
 // One new token per sequence is exactly paged decode.
 //
-// A tile is 128 query rows: TQ = floor(128 / G) consecutive new tokens times the G
-// query heads of one KV head, row r = token * G + head (rows past TQ * G are padding).
-// A work item is a PAIR of consecutive tiles of one (sequence, KV head): both tiles
-// consume the same K/V chunks, so each chunk is read once for 256 query rows.  Per
-// 64-key chunk and tile:
-//   S[128 rows x 64 keys] = Q . K^T            (M=128, N=64,  K=128 dims)
-//   O[128 rows x 128 dims] += P . V            (M=128, N=128, K=64 keys), twice:
-// the probabilities as hi = round(p) and lo = round(p - hi) in the cache dtype, so
-// the 16-bit operand costs about 2^-17 relative per weight.  S (double-buffered) and
-// O of each tile live in TMEM; the MMA accumulates O over the item's chunks.  Softmax
-// is row-local (no cross-thread reduction) with a lazy rescale: a row keeps the
-// maximum it used for its probabilities until a chunk brings a score more than 8
-// (log2 units) above it -- probabilities stay <= 256 -- and only then is its O row
-// rescaled in TMEM.
+// A tile is 128 query rows of one KV head: its G query heads times TQ = 8 * floor(16 / G)
+// consecutive new tokens, head-major (row r = head * TQ + token; rows past G * TQ are
+// padding).  Every 8-row group is then 8 tokens of one head, which one TMA box loads in
+// the 128-byte swizzled operand layout.  A work item is a PAIR of consecutive tiles of
+// one (sequence, KV head): both consume the same K/V chunks, so each chunk is read once
+// for 256 query rows.  Per 64-key chunk and tile:
+//   S[128 rows x 64 keys] = Q . K^T             (M=128, N=64,  K=128 dims)
+//   O[128 rows x 128 dims] += P . V             (M=128, N=128, K=64 keys), twice:
+// the probabilities as hi = round(p) and lo = round(p - hi) in the cache dtype, so the
+// 16-bit operand costs about 2^-17 relative per weight.  S (double-buffered) and O of
+// each tile live in TMEM; the probabilities are written back over the S columns they
+// came from and the PV products read them from TMEM, so shared memory holds only K/V
+// and Q.  Softmax is row-local (one thread per row, no cross-thread reduction) with a
+// lazy rescale: a row keeps the maximum it used for its probabilities until a chunk
+// brings a score more than 8 (log2 units) above it -- probabilities stay <= 256 -- and
+// only then is its O row rescaled in TMEM.
 //
-// Roles (320 threads, persistent CTAs over a longest-first work list dealt in snake
-// order):
+// Roles (320 threads, persistent CTAs over a work list in which a sequence's items are
+// adjacent -- they share K/V, which then stays in L2 -- and sequences come longest
+// first, dealt in snake order):
 //  * warps 0-3 and 4-7: one softmax warpgroup per tile of the pair (thread = query
-//    row = TMEM lane); while one group computes probabilities the tensor cores work
-//    for the other.
-//  * warp 8, producer: loads both tiles' query rows (plain loads, written in the
-//    128-byte swizzled operand layout), then per chunk one 4-D TMA box per block for
-//    K and one for V into a 3-stage ring (blocks past the pair's last position are
-//    loaded from outside the tensor: zero fill).
+//    row = TMEM lane); the two groups and the tensor cores work concurrently.
+//  * warp 8, producer: per item the query boxes of both tiles into a double buffer,
+//    then per chunk one 4-D TMA box per block for K and one for V into a 3-stage ring
+//    (blocks past the pair's last position come from outside the tensor: zero fill).
 //  * warp 9, MMA: one lane polls four streams -- QK and PV of each tile -- and issues
-//    whatever is ready; a ring stage is released once both tiles' PVs of its chunk
-//    are issued (their commit fires when they complete).
+//    whatever is ready; a ring stage is released once both tiles' PVs of its chunk are
+//    issued (their commit fires when they complete).  tcgen05 MMAs of one thread run
+//    in issue order, so QK(c + 2) may overwrite the probabilities of chunk c once
+//    PV(c) has been issued.
 #include <climits>
 #include <type_traits>
 
@@ -57,28 +60,25 @@ constexpr int kGroup = 2048;               // 8-row group of a 128-dim tile: two
 constexpr int kKVTile = kKC * 256;         // K (or V) of one chunk: 16 KB
 constexpr int kStageBytes = 2 * kKVTile;   // K then V
 constexpr int kQBytes = kRows * 256;       // 32 KB per tile: [16 groups][2 halves][8 rows][128 B]
-constexpr int kPPart = kRows * kKC * 2;    // 16 KB: [16 groups][8 rows][128 B], one part
-constexpr int kPBytes = 2 * kPPart;        // per tile: hi part then lo part
+constexpr int kQItem = kGroups * kQBytes;  // both tiles of an item
 constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kOffP = kOffQ + kGroups * kQBytes;
-constexpr int kOffBar = kOffP + kGroups * kPBytes;
-// ring full/empty, qfull, qempty, then per tile: sfull[2], sfree[2], pfull, pvdone[2]; drain
-constexpr int kNumBars = 2 * kStages + 2 + kGroups * 7 + 1;
+constexpr int kOffBar = kOffQ + 2 * kQItem;
+// ring full/empty, qfull[2], qempty[2], then per tile: sfull[2], pfull[2], pvdone[2]; drain
+constexpr int kNumBars = 2 * kStages + 4 + kGroups * 6 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;        // per tile g: S[2] at 256g + 0/64, O at 256g + 128
 constexpr float kRescaleSlack = 8.f;       // log2 units a row's max may grow before O is rescaled
 constexpr int kListThreads = 1024;
 constexpr int kMaxBuckets = 1024;          // chunk-count buckets of the work list (last one open-ended)
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Bars {
-  uint64_t *full, *empty, *qfull, *qempty, *drain, *grp;
-  // per tile g: sfull[2], sfree[2], pfull, pvdone[2] (addresses computed, so a
-  // runtime tile index needs no local-memory table)
-  __device__ __forceinline__ uint64_t* sfull(int g, int i) const { return grp + 7 * g + i; }
-  __device__ __forceinline__ uint64_t* sfree(int g, int i) const { return grp + 7 * g + 2 + i; }
-  __device__ __forceinline__ uint64_t* pfull(int g) const { return grp + 7 * g + 4; }
-  __device__ __forceinline__ uint64_t* pvdone(int g, int i) const { return grp + 7 * g + 5 + i; }
+  uint64_t *full, *empty, *qfull, *qempty, *grp, *drain;
+  // per tile g (addresses computed, so a runtime tile index needs no local-memory table)
+  __device__ __forceinline__ uint64_t* sfull(int g, int i) const { return grp + 6 * g + i; }
+  __device__ __forceinline__ uint64_t* pfull(int g, int i) const { return grp + 6 * g + 2 + i; }
+  __device__ __forceinline__ uint64_t* pvdone(int g, int i) const { return grp + 6 * g + 4 + i; }
 };
 
 __device__ __forceinline__ Bars carve(unsigned char* smem) {
@@ -87,19 +87,20 @@ __device__ __forceinline__ Bars carve(unsigned char* smem) {
   r.full = b;
   r.empty = b + kStages;
   r.qfull = b + 2 * kStages;
-  r.qempty = r.qfull + 1;
-  r.grp = r.qempty + 1;
-  r.drain = r.grp + 7 * kGroups;
+  r.qempty = r.qfull + 2;
+  r.grp = r.qempty + 2;
+  r.drain = r.grp + 6 * kGroups;
   return r;
 }
 
 struct PrefillArgs {
   CUtensorMap tk;  // pool 4-D views: one box = one block's tile for one KV head
   CUtensorMap tv;
+  CUtensorMap tq;  // queries (128 dims, heads, tokens): one box = 8 tokens x 64 dims of one head
   PrefillParams p;
 };
 
-// {s, g | ntile_a << 12 | ntile_b << 20, first query row of tile a, position of its first token}
+// {s, g | ntile_a << 12 | ntile_b << 20, first query token of tile a, position of that token}
 struct Item {
   int s, g, na, nb, qrow0, pos0, last, nchunks;  // na, nb: tokens in tile a, tile b
   __device__ __forceinline__ int ntok(int tile) const { return tile ? nb : na; }
@@ -118,14 +119,27 @@ __device__ __forceinline__ Item unpack_item(int4 e, int tq) {
   return t;
 }
 
-// byte offset of 16-byte piece `c16` (0..15 over 128 dims) of row r in a
-// [group][half][8 rows][128 B] tile with 128-byte swizzle
-__device__ __forceinline__ int swz_dims(int r, int c16) {
-  return (r >> 3) * kGroup + (c16 >> 3) * 1024 + (r & 7) * 128 + (((c16 & 7) ^ (r & 7)) << 4);
-}
-// same for a [group][8 rows][128 B] tile of 64 keys (one half)
-__device__ __forceinline__ int swz_keys(int r, int c16) {
-  return (r >> 3) * 1024 + (r & 7) * 128 + (((c16 & 7) ^ (r & 7)) << 4);
+// Extreme of this thread's 64 raw scores of S (maximum, or minimum when the scale is
+// negative), keys past `lim` excluded when the chunk crosses the diagonal.
+template <bool kMin>
+__device__ __forceinline__ float chunk_extreme(uint32_t taddr, bool diagonal, int lim) {
+  constexpr float kNone = kMin ? INFINITY : -INFINITY;
+  float e0 = kNone, e1 = kNone;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float sv[32];
+    tmem_load32(taddr + h * 32, sv);
+    if (diagonal) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sv[i] = h * 32 + i <= lim ? sv[i] : kNone;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      e0 = kMin ? fmin3(e0, sv[i], sv[i + 1]) : fmax3(e0, sv[i], sv[i + 1]);
+      e1 = kMin ? fmin3(e1, sv[i + 2], sv[i + 3]) : fmax3(e1, sv[i + 2], sv[i + 3]);
+    }
+  }
+  return kMin ? fminf(e0, e1) : fmaxf(e0, e1);
 }
 
 template <typename T>
@@ -138,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);
   int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);
+  int* qissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 16);
   const int G = p.group, TQ = p.tile_tokens;
   const int num_items = *p.work_count;
 
@@ -146,19 +161,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&bars.full[i], 1);
       mbar_init(&bars.empty[i], 1);
     }
-    mbar_init(bars.qfull, 1);
-    mbar_init(bars.qempty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.qfull[i], 1);
+      mbar_init(&bars.qempty[i], 1);
+    }
     for (int g = 0; g < kGroups; ++g) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(bars.sfull(g, i), 1);
-        mbar_init(bars.sfree(g, i), 4);
+        mbar_init(bars.pfull(g, i), 4);
         mbar_init(bars.pvdone(g, i), 1);
       }
-      mbar_init(bars.pfull(g), 4);
     }
     *abort_flag = 0;
     *issued_slot = 0;
     *waited_slot = 0;
+    *qissued_slot = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
@@ -172,40 +189,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (lane == 0) {
       prefetch_tensormap(&a.tk);
       prefetch_tensormap(&a.tv);
+      prefetch_tensormap(&a.tq);
     }
-    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_normal();  // K/V: re-read by the sequence's other items
+    const uint64_t pol_q = policy_evict_first();    // Q: read once
     const int bs = p.block_size;
     const int blocks_per_chunk = kKC / bs;
     const int oob_group = p.num_blocks * p.num_kv_heads * bs / 8;  // first row group outside the pool
+    // this lane's query box of a tile: 8-row group lane / 2, half lane % 2
+    const int qrows = (lane >> 1) * 8, qhalf = lane & 1;
+    const int qhead = qrows / TQ, qtok = qrows % TQ;
     int c = 0, j = 0;
     bool ok = true;
     ItemCursor cur;
     for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance(), ++j) {
       const Item it = unpack_item(cur.cur, TQ);
-      // ---- both tiles' query rows, swizzled, zero past each tile; the previous
-      //      item's QKs must be done with the buffers ----
-      ok = j < 1 || __shfl_sync(0xffffffffu, lane == 0 ? wait_role(bars.qempty, (j - 1) & 1, abort_flag, p.err)
-                                                       : true, 0);
-      if (!ok) break;
-#pragma unroll 1
-      for (int g = 0; g < kGroups; ++g) {
-        unsigned char* qbuf = smem + kOffQ + g * kQBytes;
-        const int valid_rows = it.ntok(g) * G;
-#pragma unroll 1
-        for (int r = lane; r < kRows; r += 32) {
-          const bool valid = r < valid_rows;
-          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-              (static_cast<size_t>(it.qrow0 + g * TQ + r / G) * p.num_q_heads + it.g * G + r % G) * 128);
-#pragma unroll
-          for (int c16 = 0; c16 < 16; ++c16) {
-            const uint4 v = valid ? src[c16] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(qbuf + swz_dims(r, c16)) = v;
-          }
-        }
+      // ---- both tiles' queries into buffer j & 1 (free once item j - 2's QKs completed) ----
+      const int qb = j & 1;
+      if (lane == 0) {
+        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err);
+        if (ok) mbar_arrive_expect_tx(&bars.qfull[qb], kQItem);
       }
-      fence_proxy_async_smem();
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.qfull);
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        // padding groups (past the G heads) read tokens outside the tensor: zeros
+        const int tok = qhead < G ? it.qrow0 + g * TQ + qtok : p.num_query_tokens;
+        const int head = it.g * G + min(qhead, G - 1);
+        tma_load_3d(smem + kOffQ + qb * kQItem + g * kQBytes + (lane >> 1) * kGroup + qhalf * 1024, &a.tq,
+                    qhalf * 64, head, tok, &bars.qfull[qb], pol_q);
+      }
+      if (lane == 0) *qissued_slot = j + 1;
       // ---- K/V chunks ----
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
@@ -230,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             grp = (b * p.num_kv_heads + it.g) * bs / 8;
           }
           unsigned char* dst = smem + st * kStageBytes + lane * bs * 256;
-          tma_load_4d(dst, &a.tk, grp, &bars.full[st], pol_stream);
-          tma_load_4d(dst + kKVTile, &a.tv, grp, &bars.full[st], pol_stream);
+          tma_load_4d(dst, &a.tk, grp, &bars.full[st], pol_kv);
+          tma_load_4d(dst + kKVTile, &a.tv, grp, &bars.full[st], pol_kv);
         }
         if (lane == 0) *issued_slot = c + 1;
       }
@@ -244,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, false, true, kRows, 128);
       const uint32_t ring = smem_addr(smem);
       const uint32_t qbase = smem_addr(smem + kOffQ);
-      const uint32_t pbase = smem_addr(smem + kOffP);
       // one cursor per stream: QK and PV of each tile walk the same chunk sequence
       struct Stream {
         ItemCursor cur;
@@ -267,8 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           s.n = s.cur.valid() ? unpack_item(s.cur.cur, TQ).nchunks : 0;
         }
       };
-      int q_items = 0;     // items whose query buffers both tiles are done with
-      int q_last = 0;      // tiles that issued the current item's last QK
+      int ql0 = 0, ql1 = 0;  // per query buffer: tiles that issued the item's last QK
       uint64_t idle_since = global_timer_ns();
       while (true) {
         bool active = false, progressed = false;
@@ -277,15 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           Stream& s = qs[g];
           if (!s.cur.valid()) continue;
           active = true;
-          if (s.cur.k != q_items) continue;  // one query buffer per tile: no running ahead
+          const int jq = s.cur.k, qb = jq & 1;
           const int c = s.c, st = c % kStages, sb = c & 1;
-          if ((s.k > 0 || mbar_try_wait(bars.qfull, q_items & 1)) &&
-              mbar_try_wait(&bars.full[st], (c / kStages) & 1) &&
-              (c < 2 || mbar_try_wait(bars.sfree(g, sb), ((c >> 1) - 1) & 1))) {
+          // S buffer sb held the probabilities of chunk c - 2: PV(c - 2) must be issued
+          if (ps[g].c >= c - 1 && (s.k > 0 || mbar_try_wait(&bars.qfull[qb], (jq >> 1) & 1)) &&
+              mbar_try_wait(&bars.full[st], (c / kStages) & 1)) {
             if (g == 0) *waited_slot = c + 1;
             tc_fence_after();
             const uint32_t kb = ring + st * kStageBytes;
-            const uint32_t qa = qbase + g * kQBytes;
+            const uint32_t qa = qbase + qb * kQItem + g * kQBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 32;
@@ -293,10 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                       smem_desc(kb + off, 16, kGroup, kLayoutSwizzle128), idesc_qk, kk > 0);
             }
             mma_commit(bars.sfull(g, sb));
-            if (s.k == s.n - 1 && ++q_last == kGroups) {  // both tiles' queries consumed
-              mma_commit(bars.qempty);
-              q_last = 0;
-              ++q_items;
+            if (s.k == s.n - 1) {  // this tile is done with the item's queries
+              int& ql = qb ? ql1 : ql0;
+              if (++ql == kGroups) {
+                mma_commit(&bars.qempty[qb]);
+                ql = 0;
+              }
             }
             step(s);
             progressed = true;
@@ -308,19 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (!s.cur.valid()) continue;
           active = true;
           if (s.c >= qs[g].c) continue;  // its QK comes first
-          const int c = s.c, st = c % kStages;
-          if (mbar_try_wait(bars.pfull(g), c & 1)) {
+          const int c = s.c, st = c % kStages, sb = c & 1;
+          if (mbar_try_wait(bars.pfull(g, sb), (c >> 1) & 1)) {
             tc_fence_after();
             const uint32_t vbase = ring + st * kStageBytes + kKVTile;
-            const uint32_t pa = pbase + g * kPBytes;
+            const uint32_t pa = tmem + g * 256 + sb * 64;  // probabilities: [hi 8 | lo 8] columns per 16 keys
             const uint32_t od = tmem + g * 256 + 128;
 #pragma unroll
             for (int kk = 0; kk < kKC / 16; ++kk) {
               const uint64_t bd = smem_desc(vbase + kk * 2 * kGroup, 1024, kGroup, kLayoutSwizzle128);
-              mma_f16(od, smem_desc(pa + kk * 32, 16, 1024, kLayoutSwizzle128), bd, idesc_pv, s.k > 0 || kk > 0);
-              mma_f16(od, smem_desc(pa + kPPart + kk * 32, 16, 1024, kLayoutSwizzle128), bd, idesc_pv, true);
+              mma_f16_tmem_a(od, pa + kk * 16, bd, idesc_pv, s.k > 0 || kk > 0);
+              mma_f16_tmem_a(od, pa + kk * 16 + 8, bd, idesc_pv, true);
             }
-            mma_commit(bars.pvdone(g, c & 1));
+            mma_commit(bars.pvdone(g, sb));
             // the stage is free once every tile's PV of this chunk has completed
             bool all = true;
 #pragma unroll
@@ -350,14 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int grp = warp / 4;                 // which tile of the pair
     const int t = threadIdx.x % 128;          // query row of the tile = TMEM lane
     const int wq = warp % 4;                  // lane quarter
+    const int head = t / TQ, tok = t % TQ;    // head-major rows
     const uint32_t lane_base = tmem + grp * 256 + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t obuf = lane_base + 128;
+    const bool neg_scale = p.scale_log2 < 0.f;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 mone2 = make_float2(-1.f, -1.f);
     int c = 0;
     bool ok = true;
     int prev_row = -1, prev_c = -1;
     float prev_l = 1.f;
 
-    // Warp-uniform: has this tile's PV of chunk cc completed?  (waited in chunk order)
+    // Warp-uniform: has this tile's PV of chunk cc completed?
     auto pv_done = [&](int cc) -> bool {
       return __all_sync(0xffffffffu, wait_role(bars.pvdone(grp, cc & 1), (cc >> 1) & 1, abort_flag, p.err));
     };
@@ -366,19 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       tc_fence_after();
       const float inv = 1.f / lsum;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float o[16];
-        tmem_load16(obuf + q * 16, o);
+      for (int q = 0; q < 4; ++q) {
+        float o[32];
+        tmem_load32(obuf + q * 32, o);
         if (row >= 0) {
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(row) * 128 + q * 16);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(row) * 128 + q * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + static_cast<size_t>(row) * 128 + q * 16);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + static_cast<size_t>(row) * 128 + q * 32);
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pack2<T>(o[8 * i] * inv, o[8 * i + 1] * inv),
                                   pack2<T>(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
                                   pack2<T>(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
@@ -392,35 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     ItemCursor cur;
     for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
       const Item it = unpack_item(cur.cur, TQ);
-      const int valid_rows = it.ntok(grp) * G;
-      const bool row_valid = t < valid_rows;
-      const int qpos = row_valid ? it.pos0 + grp * TQ + t / G : it.last;  // padding rows act as the last token
-      const int out_row = row_valid ? (it.qrow0 + grp * TQ + t / G) * p.num_q_heads + it.g * G + t % G : -1;
+      const bool row_valid = head < G && tok < it.ntok(grp);
+      const int qpos = row_valid ? it.pos0 + grp * TQ + tok : it.last;  // padding rows act as the last token
+      const int out_row = row_valid ? (it.qrow0 + grp * TQ + tok) * p.num_q_heads + it.g * G + head : -1;
       float m = 0.f, l = 0.f;  // max used for this row's probabilities, running row sum
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
+        const uint32_t sbuf = lane_base + sb * 64;
         if (!__all_sync(0xffffffffu, wait_role(bars.sfull(grp, sb), (c >> 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int kbase = k * kKC;
-        const bool diagonal = kbase + kKC - 1 > qpos;  // only then does the mask cut this row
-        // pass 1: the row's chunk max under the causal mask (16-column pieces of S)
-        float cm = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kKC / 16; ++q) {
-          float sv[16];
-          tmem_load16(lane_base + sb * 64 + q * 16, sv);
-          if (diagonal) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (kbase + q * 16 + i <= qpos) cm = fmaxf(cm, sv[i] * p.scale_log2);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) cm = fmaxf(cm, sv[i] * p.scale_log2);
-          }
-        }
+        const int lim = qpos - kbase;            // keys of the chunk past lim are masked
+        const bool diagonal = lim < kKC - 1;     // only then does the mask cut this row
+        // pass 1: the row's chunk maximum of scale * score under the mask
+        const float cm = (neg_scale ? chunk_extreme<true>(sbuf, diagonal, lim)
+                                    : chunk_extreme<false>(sbuf, diagonal, lim)) * p.scale_log2;
         // lazy rescale: keep m unless the chunk brings a score more than the slack above
         // (a chunk entirely past this row's position gives cm = -inf and changes nothing)
         float alpha = 1.f;
@@ -431,17 +440,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           m = cm;
           l *= alpha;
         }
-        // the previous chunk's PV (reads P, accumulates O) must be done before P is
-        // rewritten, O rescaled, or -- at an item's first chunk -- O read out
-        if (c >= 1 && !pv_done(c - 1)) {
-          ok = false;
-          break;
-        }
+        // O is read out (at an item's first chunk) or rescaled only after the PVs that
+        // accumulate it have completed
         if (k == 0 && prev_c >= 0) {
+          if (!pv_done(prev_c)) {
+            ok = false;
+            break;
+          }
           finish(prev_row, prev_l);
           prev_c = -1;
         }
         if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!pv_done(c - 1)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 1
           for (int q = 0; q < 8; ++q) {
@@ -451,42 +464,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             for (int i = 0; i < 16; ++i) o[i] *= alpha;
             tmem_store16(obuf + q * 16, o);
           }
-          tc_fence_before();
         }
-        // pass 2: probabilities as hi + lo parts into P's swizzled rows
-        float rowsum = 0.f;
-        unsigned char* ph = smem + kOffP + grp * kPBytes;
-        const float neg_m = -m;
+        // pass 2: probabilities as hi + lo parts, written over the 16 S columns they
+        // came from: [hi of 16 keys | lo of 16 keys]
+        float2 acc = make_float2(0.f, 0.f);
+        const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
           float sv[16];
-          tmem_load16(lane_base + sb * 64 + q * 16, sv);
+          tmem_load16(sbuf + q * 16, sv);
+          uint32_t w[16];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const int jj = q * 16 + half * 8 + i;
-              float p0 = exp2_approx(fmaf(sv[half * 8 + i], p.scale_log2, neg_m));
-              float p1 = exp2_approx(fmaf(sv[half * 8 + i + 1], p.scale_log2, neg_m));
-              if (diagonal) {
-                p0 = kbase + jj <= qpos ? p0 : 0.f;
-                p1 = kbase + jj + 1 <= qpos ? p1 : 0.f;
-              }
-              rowsum += p0 + p1;
-              float h0, h1;
-              hw[i / 2] = pack2_split<T>(p0, p1, h0, h1);  // rounded pair, and its values
-              lw[i / 2] = pack2<T>(p0 - h0, p1 - h1);      // exact remainders, rounded
+          for (int i = 0; i < 8; ++i) {
+            const float2 x = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
+            float p0 = exp2_approx(x.x), p1 = exp2_approx(x.y);
+            if (diagonal) {
+              p0 = q * 16 + 2 * i <= lim ? p0 : 0.f;
+              p1 = q * 16 + 2 * i + 1 <= lim ? p1 : 0.f;
             }
-            const int off = swz_keys(t, q * 2 + half);
-            *reinterpret_cast<uint4*>(ph + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(ph + kPPart + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            const float2 pr = make_float2(p0, p1);
+            float h0, h1;
+            w[i] = pack2_split<T>(p0, p1, h0, h1);                               // rounded pair
+            const float2 lo = __ffma2_rn(make_float2(h0, h1), mone2, pr);       // exact remainders
+            w[8 + i] = pack2<T>(lo.x, lo.y);
+            acc = __fadd2_rn(acc, pr);
           }
+          tmem_store16_words(sbuf + q * 16, w);
         }
-        l += rowsum;
+        l += acc.x + acc.y;
+        tmem_store_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.sfree(grp, sb));
         // V rows past the pair's last position inside loaded blocks: zero them (a NaN
         // there would survive a zero weight).  Both groups write the same zeros.
         const int rows_needed = it.last + 1 - kbase;
@@ -500,10 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
               reinterpret_cast<uint4*>(vrow + 1024)[q] = make_uint4(0, 0, 0, 0);
             }
           }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.pfull(grp));
+        if (lane == 0) mbar_arrive(bars.pfull(grp, sb));
       }
       if (!ok) break;
       prev_row = out_row;
@@ -520,6 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (warp == kProducerWarp && lane == 0) {
       for (int c = *waited_slot; c < *issued_slot; ++c)
         if (!mbar_wait(&bars.full[c % kStages], (c / kStages) & 1)) break;
+      for (int jj = max(0, *qissued_slot - 2); jj < *qissued_slot; ++jj)
+        if (!mbar_wait(&bars.qfull[jj & 1], (jj >> 1) & 1)) break;
     }
     if (warp == kMmaWarp && lane == 0) {
       mbar_init(bars.drain, 1);
@@ -534,8 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Work list: one entry per (sequence, KV head, pair of query tiles), sorted by chunk
-// count, longest first (counting sort; order inside one count does not matter).
+// Work list: one entry per (sequence, KV head, pair of query tiles).  A sequence's
+// entries are adjacent (head by head, pairs in order) so the CTAs working on them at
+// the same time share its K/V through L2; sequences are ordered by chunk count,
+// longest first (counting sort over sequences).
 __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid_constant__ PrefillParams p) {
   __shared__ int hist[kMaxBuckets];
   __shared__ int next[kMaxBuckets];
@@ -548,10 +559,7 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
       set_error(p.err, kErrLength);
       continue;
     }
-    for (int t0 = 0; t0 < n; t0 += span) {
-      const int nch = (L - n + t0 + min(span, n - t0) + kKC - 1) / kKC;
-      atomicAdd(&hist[min(nch, kMaxBuckets - 1)], H);
-    }
+    if (n > 0) atomicAdd(&hist[min((L + kKC - 1) / kKC, kMaxBuckets - 1)], (n + span - 1) / span * H);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -565,15 +573,30 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
     const int n = p.query_start[s + 1] - p.query_start[s], L = p.context_lens[s];
-    if (n < 0 || L < n || L > p.max_context_len) continue;
-    for (int t0 = 0; t0 < n; t0 += span) {
-      const int na = min(TQ, n - t0), nb = max(0, min(TQ, n - t0 - TQ));
-      const int nch = (L - n + t0 + na + nb + kKC - 1) / kKC;
-      const int pos = atomicAdd(&next[min(nch, kMaxBuckets - 1)], H);
-      for (int g = 0; g < H; ++g)
-        p.work_list[pos + g] = make_int4(s, g | (na << 12) | (nb << 20), p.query_start[s] + t0, L - n + t0);
-    }
+    if (n <= 0 || L < n || L > p.max_context_len) continue;
+    const int pairs = (n + span - 1) / span;
+    int pos = atomicAdd(&next[min((L + kKC - 1) / kKC, kMaxBuckets - 1)], pairs * H);
+    for (int g = 0; g < H; ++g)
+      for (int i = pairs - 1; i >= 0; --i) {  // longest pair first
+        const int t0 = i * span;
+        const int na = min(TQ, n - t0), nb = max(0, min(TQ, n - t0 - TQ));
+        p.work_list[pos++] = make_int4(s, g | (na << 12) | (nb << 20), p.query_start[s] + t0, L - n + t0);
+      }
   }
+}
+
+// Queries [tokens][heads][128] seen as 3-D (128 dims, heads, tokens); a box is 8
+// tokens x 64 dims of one head, landing as one swizzled 8-row group half.
+bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, heads, tokens};
+  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
+  cuuint32_t box[3] = {64, 1, 8};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q),
+            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename T>
@@ -591,21 +614,23 @@ cudaError_t launch_prefill_t(const PrefillArgs& args, int grid, cudaStream_t str
 
 }  // namespace
 
-int prefill_tile_tokens(int group) { return kRows / group; }
+int prefill_tile_tokens(int group) { return 8 * (kRows / 8 / group); }
 
 size_t prefill_max_items(int num_seqs, int num_query_tokens, int num_kv_heads, int group) {
-  const int span = kGroups * (kRows / group);
+  const int span = kGroups * prefill_tile_tokens(group);
   return (static_cast<size_t>(num_query_tokens) / span + num_seqs) * num_kv_heads;
 }
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t stream) {
   if (p.num_kv_heads > 4095) return cudaErrorInvalidValue;  // packed into 12 bits of a list entry
+  if (p.group < 1 || p.group > 16 || p.num_query_tokens <= 0) return cudaErrorInvalidValue;
   PrefillArgs args;
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
   if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
-      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16))
+      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
+      !make_query_map(&args.tq, p.q, p.num_q_heads, p.num_query_tokens, bf16))
     return cudaErrorInvalidValue;
   prefill_list_kernel<<<1, kListThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();

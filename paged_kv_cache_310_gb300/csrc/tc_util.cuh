@@ -101,6 +101,18 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// Three-input maximum / minimum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <typename T>
 __device__ __forceinline__ float round_to(float x) {
   return Elem<T>::to_float(Elem<T>::from_float(x));

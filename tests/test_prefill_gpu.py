@@ -17,6 +17,8 @@ CASES = [
     ("bf16", 32, 16, 1, 600, 1, None), ("f16", 16, 12, 4, 500, 1, None), ("bf16", 16, 32, 2, 400, 1, None),
     ("bf16", 16, 8, 2, 2000, 1500, lambda s, L: 128), ("f16", 32, 32, 8, 1200, 1, lambda s, L: (s * 37) % 5),
     ("bf16", 8, 4, 4, 3000, 2000, lambda s, L: L),
+    # query-head groups that do not divide 16: 5, 6 and 7 heads per KV head
+    ("bf16", 16, 40, 8, 800, 1, None), ("f16", 16, 12, 2, 600, 100, None), ("bf16", 32, 28, 4, 900, 200, None),
 ]
 
 
