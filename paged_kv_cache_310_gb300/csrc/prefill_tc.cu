@@ -51,20 +51,21 @@ namespace pkv {
 namespace {
 
 constexpr int kGroups = 2;                 // tiles per item, one softmax warpgroup each
-constexpr int kThreads = (4 * kGroups + 2) * 32;
-constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = 4 * kGroups + 1;
+constexpr int kThreads = (4 * kGroups + 3) * 32;
+constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = 4 * kGroups + 1, kVWarp = 4 * kGroups + 2;
 constexpr int kRows = 128;                 // query rows per tile (M)
 constexpr int kKC = 64;                    // keys per chunk
-constexpr int kStages = 3;
+constexpr int kStages = 3;                 // per ring (K and V have one each)
 constexpr int kGroup = 2048;               // 8-row group of a 128-dim tile: two 64-column halves
 constexpr int kKVTile = kKC * 256;         // K (or V) of one chunk: 16 KB
-constexpr int kStageBytes = 2 * kKVTile;   // K then V
 constexpr int kQBytes = kRows * 256;       // 32 KB per tile: [16 groups][2 halves][8 rows][128 B]
 constexpr int kQItem = kGroups * kQBytes;  // both tiles of an item
-constexpr int kOffQ = kStages * kStageBytes;
+constexpr int kOffV = kStages * kKVTile;
+constexpr int kOffQ = 2 * kStages * kKVTile;
 constexpr int kOffBar = kOffQ + 2 * kQItem;
-// ring full/empty, qfull[2], qempty[2], then per tile: sfull[2], pfull[2], pvdone[2]; drain
-constexpr int kNumBars = 2 * kStages + 4 + kGroups * 6 + 1;
+// K ring full/empty, V ring full/empty, qfull[2], qempty[2], then per tile: sfull[2],
+// pfull[2], pvdone[2]; drain
+constexpr int kNumBars = 4 * kStages + 4 + kGroups * 6 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;        // per tile g: S[2] at 256g + 0/64, O at 256g + 128
@@ -74,7 +75,7 @@ constexpr int kMaxBuckets = 1024;          // chunk-count buckets of the work li
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Bars {
-  uint64_t *full, *empty, *qfull, *qempty, *grp, *drain;
+  uint64_t *kfull, *kempty, *vfull, *vempty, *qfull, *qempty, *grp, *drain;
   // per tile g (addresses computed, so a runtime tile index needs no local-memory table)
   __device__ __forceinline__ uint64_t* sfull(int g, int i) const { return grp + 6 * g + i; }
   __device__ __forceinline__ uint64_t* pfull(int g, int i) const { return grp + 6 * g + 2 + i; }
@@ -84,9 +85,11 @@ struct Bars {
 __device__ __forceinline__ Bars carve(unsigned char* smem) {
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
   Bars r;
-  r.full = b;
-  r.empty = b + kStages;
-  r.qfull = b + 2 * kStages;
+  r.kfull = b;
+  r.kempty = b + kStages;
+  r.vfull = b + 2 * kStages;
+  r.vempty = b + 3 * kStages;
+  r.qfull = b + 4 * kStages;
   r.qempty = r.qfull + 2;
   r.grp = r.qempty + 2;
   r.drain = r.grp + 6 * kGroups;
@@ -119,27 +122,62 @@ __device__ __forceinline__ Item unpack_item(int4 e, int tq) {
   return t;
 }
 
-// Extreme of this thread's 64 raw scores of S (maximum, or minimum when the scale is
-// negative), keys past `lim` excluded when the chunk crosses the diagonal.
+// Extreme of a row's 64 raw scores (maximum, or minimum when the scale is negative),
+// keys past `lim` excluded when the chunk crosses the diagonal (overwritten in place
+// with the neutral value).
 template <bool kMin>
-__device__ __forceinline__ float chunk_extreme(uint32_t taddr, bool diagonal, int lim) {
+__device__ __forceinline__ float chunk_extreme(float* sv, bool diagonal, int lim) {
   constexpr float kNone = kMin ? INFINITY : -INFINITY;
+  if (diagonal) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) sv[i] = i <= lim ? sv[i] : kNone;
+  }
   float e0 = kNone, e1 = kNone;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float sv[32];
-    tmem_load32(taddr + h * 32, sv);
-    if (diagonal) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sv[i] = h * 32 + i <= lim ? sv[i] : kNone;
-    }
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      e0 = kMin ? fmin3(e0, sv[i], sv[i + 1]) : fmax3(e0, sv[i], sv[i + 1]);
-      e1 = kMin ? fmin3(e1, sv[i + 2], sv[i + 3]) : fmax3(e1, sv[i + 2], sv[i + 3]);
-    }
+  for (int i = 0; i < 64; i += 4) {
+    e0 = kMin ? fmin3(e0, sv[i], sv[i + 1]) : fmax3(e0, sv[i], sv[i + 1]);
+    e1 = kMin ? fmin3(e1, sv[i + 2], sv[i + 3]) : fmax3(e1, sv[i + 2], sv[i + 3]);
   }
   return kMin ? fminf(e0, e1) : fmaxf(e0, e1);
+}
+
+// One producer warp's copies of an item's chunks of K (or V) into its ring: per chunk
+// one 4-D box per block (blocks past the pair's last position from outside the tensor:
+// zero fill).  `c` counts the warp's chunks over all items.  Returns false on abort.
+__device__ __forceinline__ bool load_chunks(const PrefillParams& p, const Item& it, const CUtensorMap* map,
+                                            unsigned char* ring, uint64_t* full, uint64_t* empty, int& c,
+                                            int* issued_slot, uint64_t policy, volatile int* abort_flag) {
+  const int lane = threadIdx.x % 32;
+  const int bs = p.block_size;
+  const int blocks_per_chunk = kKC / bs;
+  const int oob_group = p.num_blocks * p.num_kv_heads * bs / 8;  // first row group outside the pool
+  const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
+  for (int k = 0; k < it.nchunks; ++k, ++c) {
+    const int st = c % kStages;
+    const int lb = k * blocks_per_chunk + lane;  // logical block of this lane
+    const bool live = lane < blocks_per_chunk && lb * bs <= it.last;
+    int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
+    bool ok = true;
+    if (lane == 0) {
+      ok = c < kStages || wait_role(&empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+      if (ok) mbar_arrive_expect_tx(&full[st], kKVTile);
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    __syncwarp();
+    if (lane < blocks_per_chunk) {
+      int grp = oob_group;
+      if (live) {
+        if (b < 0 || b >= p.num_blocks) {
+          set_error(p.err, kErrIndex);
+          b = 0;
+        }
+        grp = (b * p.num_kv_heads + it.g) * bs / 8;
+      }
+      tma_load_4d(ring + st * kKVTile + lane * bs * 256, map, grp, &full[st], policy);
+    }
+    if (lane == 0) *issued_slot = c + 1;
+  }
+  return true;
 }
 
 template <typename T>
@@ -150,16 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const Bars bars = carve(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);
+  int* kissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  int* vissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);
   int* qissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 16);
   const int G = p.group, TQ = p.tile_tokens;
   const int num_items = *p.work_count;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], 1);
+      mbar_init(&bars.kfull[i], 1);
+      mbar_init(&bars.kempty[i], 1);
+      mbar_init(&bars.vfull[i], 1);
+      mbar_init(&bars.vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.qfull[i], 1);
@@ -173,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
     }
     *abort_flag = 0;
-    *issued_slot = 0;
-    *waited_slot = 0;
+    *kissued_slot = 0;
+    *vissued_slot = 0;
     *qissued_slot = 0;
     fence_barrier_init();
   }
@@ -185,17 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kProducerWarp) {
-    // ============================ producer ============================
+    // ============================ producer: Q and K ============================
     if (lane == 0) {
       prefetch_tensormap(&a.tk);
-      prefetch_tensormap(&a.tv);
       prefetch_tensormap(&a.tq);
     }
     const uint64_t pol_kv = policy_evict_normal();  // K/V: re-read by the sequence's other items
     const uint64_t pol_q = policy_evict_first();    // Q: read once
-    const int bs = p.block_size;
-    const int blocks_per_chunk = kKC / bs;
-    const int oob_group = p.num_blocks * p.num_kv_heads * bs / 8;  // first row group outside the pool
     // this lane's query box of a tile: 8-row group lane / 2, half lane % 2
     const int qrows = (lane >> 1) * 8, qhalf = lane & 1;
     const int qhead = qrows / TQ, qtok = qrows % TQ;
@@ -222,143 +258,122 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     qhalf * 64, head, tok, &bars.qfull[qb], pol_q);
       }
       if (lane == 0) *qissued_slot = j + 1;
-      // ---- K/V chunks ----
-      const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
-      for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
-        const int st = c % kStages;
-        const int lb = k * blocks_per_chunk + lane;  // logical block of this lane
-        const bool live = lane < blocks_per_chunk && lb * bs <= it.last;
-        int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
-        if (lane == 0) {
-          ok = c < kStages || wait_role(&bars.empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
-          if (ok) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        __syncwarp();
-        if (lane < blocks_per_chunk) {
-          int grp = oob_group;
-          if (live) {
-            if (b < 0 || b >= p.num_blocks) {
-              set_error(p.err, kErrIndex);
-              b = 0;
-            }
-            grp = (b * p.num_kv_heads + it.g) * bs / 8;
-          }
-          unsigned char* dst = smem + st * kStageBytes + lane * bs * 256;
-          tma_load_4d(dst, &a.tk, grp, &bars.full[st], pol_kv);
-          tma_load_4d(dst + kKVTile, &a.tv, grp, &bars.full[st], pol_kv);
-        }
-        if (lane == 0) *issued_slot = c + 1;
-      }
+      // ---- K chunks (a stage is free once both tiles' QKs of its chunk completed) ----
+      ok = load_chunks(p, it, &a.tk, smem, bars.kfull, bars.kempty, c, kissued_slot, pol_kv, abort_flag);
+    }
+  } else if (warp == kVWarp) {
+    // ============================ producer: V ============================
+    if (lane == 0) prefetch_tensormap(&a.tv);
+    const uint64_t pol_kv = policy_evict_normal();
+    int c = 0;
+    bool ok = true;
+    ItemCursor cur;
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+      // a stage is free once both tiles' PVs of its chunk completed
+      ok = load_chunks(p, unpack_item(cur.cur, TQ), &a.tv, smem + kOffV, bars.vfull, bars.vempty, c, vissued_slot,
+                       pol_kv, abort_flag);
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ============================
-    if (lane == 0) {
-      constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-      constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kRows, kKC);
-      constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, false, true, kRows, 128);
-      const uint32_t ring = smem_addr(smem);
-      const uint32_t qbase = smem_addr(smem + kOffQ);
-      // one cursor per stream: QK and PV of each tile walk the same chunk sequence
-      struct Stream {
-        ItemCursor cur;
-        int k, n, c;  // chunk within the item, chunks in the item, global chunk
-      };
-      Stream qs[kGroups], ps[kGroups];
+    // A fixed schedule, per chunk c: PV of tile 0, PV of tile 1, then QK of both tiles
+    // for chunk c + 2 (whose S buffers held the probabilities of chunk c).  The whole
+    // warp runs it with warp-uniform control flow (descriptors and counters stay in
+    // uniform registers); one elected lane issues.
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kRows, kKC);
+    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, false, true, kRows, 128);
+    // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
+    const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, kGroup, kLayoutSwizzle128);
+    const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroup, kLayoutSwizzle128);
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), 1024, kGroup, kLayoutSwizzle128);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, wait_role(bar, parity, abort_flag, p.err));
+    };
+    // QK side: next chunk qc (global), its stage / phase, its place in the item
+    ItemCursor qcur;
+    qcur.init(p.work_list, num_items);
+    int qc = 0, qst = 0, qph = 0, qk = 0, qn = qcur.valid() ? unpack_item(qcur.cur, TQ).nchunks : 0;
+    // PV side
+    ItemCursor pcur;
+    pcur.init(p.work_list, num_items);
+    int pc = 0, pst = 0, pph = 0, pk = 0, pn = qn;
+    bool ok = true;
+    // QK of chunk qc for both tiles
+    auto qk_pair = [&]() -> bool {
+      const int qj = qcur.k, qb = qj & 1, sb = qc & 1;
+      if (qk == 0 && !wait_all(&bars.qfull[qb], (qj >> 1) & 1)) return false;
+      if (!wait_all(&bars.kfull[qst], qph)) return false;
+      const bool last = qk == qn - 1;
+      const uint64_t dk = dk0 + ((qst * kKVTile) >> 4);
+      const uint64_t dqb = dq0 + ((qb * kQItem) >> 4);
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+          const uint64_t dq = dqb + ((g * kQBytes) >> 4);
+          const uint32_t d = tmem + g * 256 + sb * 64;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            mma_f16(d, dq + off, dk + off, idesc_qk, kk > 0);
+          }
+          mma_commit(bars.sfull(g, sb));
+        }
+        mma_commit(&bars.kempty[qst]);       // both tiles' QKs of this chunk
+        if (last) mma_commit(&bars.qempty[qb]);  // both tiles are done with the item's queries
+      }
+      __syncwarp();
+      ++qc;
+      if (++qst == kStages) {
+        qst = 0;
+        qph ^= 1;
+      }
+      if (++qk == qn) {
+        qk = 0;
+        qcur.advance();
+        qn = qcur.valid() ? unpack_item(qcur.cur, TQ).nchunks : 0;
+      }
+      return true;
+    };
+    for (int i = 0; i < 2 && ok && qcur.valid(); ++i) ok = qk_pair();
+    while (ok && pcur.valid()) {
+      const int sb = pc & 1;
+      if (!wait_all(&bars.vfull[pst], pph)) break;
+      const uint64_t dv = dv0 + ((pst * kKVTile) >> 4);
+      const bool acc0 = pk > 0;
 #pragma unroll
       for (int g = 0; g < kGroups; ++g) {
-        qs[g].cur.init(p.work_list, num_items);
-        ps[g].cur.init(p.work_list, num_items);
-        qs[g].k = ps[g].k = 0;
-        qs[g].c = ps[g].c = 0;
-        qs[g].n = ps[g].n = qs[g].cur.valid() ? unpack_item(qs[g].cur.cur, TQ).nchunks : 0;
+        if (!wait_all(bars.pfull(g, sb), (pc >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t pa = tmem + g * 256 + sb * 64;  // probabilities: [hi 8 | lo 8] columns per 16 keys
+          const uint32_t od = tmem + g * 256 + 128;
+#pragma unroll
+          for (int kk = 0; kk < kKC / 16; ++kk) {
+            const uint64_t bd = dv + ((kk * 2 * kGroup) >> 4);
+            mma_f16_tmem_a(od, pa + kk * 16, bd, idesc_pv, acc0 || kk > 0);
+            mma_f16_tmem_a(od, pa + kk * 16 + 8, bd, idesc_pv, true);
+          }
+          mma_commit(bars.pvdone(g, sb));
+          if (g == kGroups - 1) mma_commit(&bars.vempty[pst]);  // every tile's PV of this chunk
+        }
+        __syncwarp();
       }
-      auto step = [&](Stream& s) {
-        ++s.c;
-        if (++s.k == s.n) {
-          s.k = 0;
-          s.cur.advance();
-          s.n = s.cur.valid() ? unpack_item(s.cur.cur, TQ).nchunks : 0;
-        }
-      };
-      int ql0 = 0, ql1 = 0;  // per query buffer: tiles that issued the item's last QK
-      uint64_t idle_since = global_timer_ns();
-      while (true) {
-        bool active = false, progressed = false;
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          Stream& s = qs[g];
-          if (!s.cur.valid()) continue;
-          active = true;
-          const int jq = s.cur.k, qb = jq & 1;
-          const int c = s.c, st = c % kStages, sb = c & 1;
-          // S buffer sb held the probabilities of chunk c - 2: PV(c - 2) must be issued
-          if (ps[g].c >= c - 1 && (s.k > 0 || mbar_try_wait(&bars.qfull[qb], (jq >> 1) & 1)) &&
-              mbar_try_wait(&bars.full[st], (c / kStages) & 1)) {
-            if (g == 0) *waited_slot = c + 1;
-            tc_fence_after();
-            const uint32_t kb = ring + st * kStageBytes;
-            const uint32_t qa = qbase + qb * kQItem + g * kQBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * 1024 + (kk & 3) * 32;
-              mma_f16(tmem + g * 256 + sb * 64, smem_desc(qa + off, 16, kGroup, kLayoutSwizzle128),
-                      smem_desc(kb + off, 16, kGroup, kLayoutSwizzle128), idesc_qk, kk > 0);
-            }
-            mma_commit(bars.sfull(g, sb));
-            if (s.k == s.n - 1) {  // this tile is done with the item's queries
-              int& ql = qb ? ql1 : ql0;
-              if (++ql == kGroups) {
-                mma_commit(&bars.qempty[qb]);
-                ql = 0;
-              }
-            }
-            step(s);
-            progressed = true;
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
-          Stream& s = ps[g];
-          if (!s.cur.valid()) continue;
-          active = true;
-          if (s.c >= qs[g].c) continue;  // its QK comes first
-          const int c = s.c, st = c % kStages, sb = c & 1;
-          if (mbar_try_wait(bars.pfull(g, sb), (c >> 1) & 1)) {
-            tc_fence_after();
-            const uint32_t vbase = ring + st * kStageBytes + kKVTile;
-            const uint32_t pa = tmem + g * 256 + sb * 64;  // probabilities: [hi 8 | lo 8] columns per 16 keys
-            const uint32_t od = tmem + g * 256 + 128;
-#pragma unroll
-            for (int kk = 0; kk < kKC / 16; ++kk) {
-              const uint64_t bd = smem_desc(vbase + kk * 2 * kGroup, 1024, kGroup, kLayoutSwizzle128);
-              mma_f16_tmem_a(od, pa + kk * 16, bd, idesc_pv, s.k > 0 || kk > 0);
-              mma_f16_tmem_a(od, pa + kk * 16 + 8, bd, idesc_pv, true);
-            }
-            mma_commit(bars.pvdone(g, sb));
-            // the stage is free once every tile's PV of this chunk has completed
-            bool all = true;
-#pragma unroll
-            for (int h = 0; h < kGroups; ++h)
-              if (h != g && ps[h].c <= c) all = false;
-            if (all) mma_commit(&bars.empty[st]);
-            step(s);
-            progressed = true;
-          }
-        }
-        if (!active) break;
-        if (progressed) {
-          idle_since = global_timer_ns();
-        } else {
-          if (*abort_flag) break;
-          if (global_timer_ns() - idle_since > kWaitLimitNs) {
-            *abort_flag = 1;
-            set_error(p.err, kErrTimeout);
-            break;
-          }
-        }
+      if (!ok) break;
+      ++pc;
+      if (++pst == kStages) {
+        pst = 0;
+        pph ^= 1;
       }
+      if (++pk == pn) {
+        pk = 0;
+        pcur.advance();
+        pn = pcur.valid() ? unpack_item(pcur.cur, TQ).nchunks : 0;
+      }
+      if (qcur.valid()) ok = qk_pair();
     }
     __syncwarp();
   } else {
@@ -427,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int kbase = k * kKC;
         const int lim = qpos - kbase;            // keys of the chunk past lim are masked
         const bool diagonal = lim < kKC - 1;     // only then does the mask cut this row
+        // the row's 64 scores, held in registers for both passes
+        float sv[64];
+        tmem_load64(sbuf, sv);
         // pass 1: the row's chunk maximum of scale * score under the mask
-        const float cm = (neg_scale ? chunk_extreme<true>(sbuf, diagonal, lim)
-                                    : chunk_extreme<false>(sbuf, diagonal, lim)) * p.scale_log2;
+        const float cm = (neg_scale ? chunk_extreme<true>(sv, diagonal, lim)
+                                    : chunk_extreme<false>(sv, diagonal, lim)) * p.scale_log2;
         // lazy rescale: keep m unless the chunk brings a score more than the slack above
         // (a chunk entirely past this row's position gives cm = -inf and changes nothing)
         float alpha = 1.f;
@@ -471,12 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
         for (int q = 0; q < kKC / 16; ++q) {
-          float sv[16];
-          tmem_load16(sbuf + q * 16, sv);
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float2 x = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), sc2, nm2);
+            const float2 x = __ffma2_rn(make_float2(sv[q * 16 + 2 * i], sv[q * 16 + 2 * i + 1]), sc2, nm2);
             float p0 = exp2_approx(x.x), p1 = exp2_approx(x.y);
             if (diagonal) {
               p0 = q * 16 + 2 * i <= lim ? p0 : 0.f;
@@ -497,10 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // V rows past the pair's last position inside loaded blocks: zero them (a NaN
         // there would survive a zero weight).  Both groups write the same zeros.
         const int rows_needed = it.last + 1 - kbase;
+        if (rows_needed < kKC) {  // warp-uniform; V of this chunk must have landed first
+          if (!__all_sync(0xffffffffu, wait_role(&bars.vfull[c % kStages], (c / kStages) & 1, abort_flag, p.err))) {
+            ok = false;
+            break;
+          }
+        }
         if (t < kKC && rows_needed < kKC) {
           const int rows_loaded = min(kKC, (rows_needed + p.block_size - 1) / p.block_size * p.block_size);
           if (t >= rows_needed && t < rows_loaded) {
-            unsigned char* vrow = smem + (c % kStages) * kStageBytes + kKVTile + (t >> 3) * kGroup + (t & 7) * 128;
+            unsigned char* vrow = smem + kOffV + (c % kStages) * kKVTile + (t >> 3) * kGroup + (t & 7) * 128;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
@@ -524,11 +546,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   // ---------------- teardown ----------------
   __syncthreads();
   if (*abort_flag) {
+    // copies still in flight land before the CTA exits: the last chunk issued on each
+    // stage (and the last query buffers) -- a phase already completed returns at once
     if (warp == kProducerWarp && lane == 0) {
-      for (int c = *waited_slot; c < *issued_slot; ++c)
-        if (!mbar_wait(&bars.full[c % kStages], (c / kStages) & 1)) break;
+      for (int c = max(0, *kissued_slot - kStages); c < *kissued_slot; ++c)
+        if (!mbar_wait(&bars.kfull[c % kStages], (c / kStages) & 1)) break;
       for (int jj = max(0, *qissued_slot - 2); jj < *qissued_slot; ++jj)
         if (!mbar_wait(&bars.qfull[jj & 1], (jj >> 1) & 1)) break;
+    }
+    if (warp == kVWarp && lane == 0) {
+      for (int c = max(0, *vissued_slot - kStages); c < *vissued_slot; ++c)
+        if (!mbar_wait(&bars.vfull[c % kStages], (c / kStages) & 1)) break;
     }
     if (warp == kMmaWarp && lane == 0) {
       mbar_init(bars.drain, 1);
