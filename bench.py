@@ -54,8 +54,12 @@ def parse():
     return ap.parse_args()
 
 
-KERNEL_SOURCES = {"tensor_core": ["common.cuh", "decode_tc.cu", "launch.h", "tcgen05.cuh"],
-                  "cuda_core": ["common.cuh", "decode_simt.cu", "launch.h"]}
+KERNEL_SOURCES = {"tensor_core": ["common.cuh", "decode_tc.cu", "launch.h", "tc_util.cuh", "tcgen05.cuh"],
+                  "cuda_core": ["common.cuh", "decode_simt.cu", "launch.h"],
+                  "prefill": ["common.cuh", "prefill_tc.cu", "launch.h", "tc_util.cuh", "tcgen05.cuh"]}
+
+
+PREFILL_WORKLOAD = "chunked prefill: 32 seqs, contexts U[1024,4096], last 512 tokens new, 64/8 heads, D128, bf16, bs16"
 
 
 def recorded_traffic(path_name, workload, partition):
@@ -270,11 +274,11 @@ def run_prefill(args):
     line = {"metric": "paged prefill attention (causal): TFLOP/s, new tokens/s", "value": tflops, "unit": "TFLOP/s",
             "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "chunked prefill: 32 seqs, contexts U[1024,4096], last 512 tokens new, "
-                                   "64/8 heads, D128, bf16, bs16", "new_tokens": int(qs[-1])},
+            "config": {"workload": PREFILL_WORKLOAD, "new_tokens": int(qs[-1])},
             "tokens_per_s": int(qs[-1]) / (ms * 1e-3),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
-                         "frac": tflops / tpeak, "peak_source": tkind, "traffic": None,
+                         "frac": tflops / tpeak, "peak_source": tkind,
+                         "traffic": recorded_traffic("prefill", PREFILL_WORKLOAD, 0),
                          "kernel": "paged_attention_prefill (work list + prefill_tc)",
                          "algorithmic_flops_per_launch": flops},
             "hbm": {"algorithmic_bytes_per_launch": kv + qo, "achieved_gbs": (kv + qo) / (ms * 1e-3) / 1e9,
