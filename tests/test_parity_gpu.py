@@ -157,6 +157,22 @@ def test_random_parity(case, path):
         check_rounded(decode_only(w, g, w.dtype, path=path, part=part), out)
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 0.6], ids=["negative", "zero", "sharp"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_scales_other_than_inverse_sqrt_d(scale, path):
+    """The scale is any finite number: a negative one turns the softmax towards the
+    smallest scores, zero gives the plain mean of the values, a large one a sharp
+    distribution dominated by a few keys."""
+    import dataclasses
+    w = workloads.random_workload(310_460, num_seqs=6, max_len=900, min_len=1, num_q_heads=16, num_kv_heads=4,
+                                  head_dim=128, block_size=16, dtype="bf16")
+    w = dataclasses.replace(w, scale=scale)
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=path, part=256)
+    check_close(out, ref, w.dtype)
+    check_rounded(decode_only(w, g, w.dtype, path=path, part=256), out)
+
+
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
 def test_empty_and_single_token_sequences(path):
     w = workloads.random_workload(99, num_seqs=12, max_len=2, min_len=0, num_q_heads=8, num_kv_heads=2,

@@ -50,6 +50,24 @@ def test_prefill_parity(case):
     assert torch.equal(low.cpu().view(torch.uint8), out.to(w.dtype).cpu().view(torch.uint8))
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 0.6], ids=["negative", "zero", "sharp"])
+def test_prefill_scales_other_than_inverse_sqrt_d(scale):
+    """A negative scale takes the minimum-score branch of the row maximum; zero gives the
+    mean of the visible values; a large scale gives a sharp distribution."""
+    w, q, qs = workloads.prefill_workload(310_960, num_seqs=5, max_len=700, min_len=1, num_q_heads=24,
+                                          num_kv_heads=4, block_size=16, dtype="bf16", new_tokens=None)
+    g = w.to("cuda")
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    pkv.paged_attention_prefill(q.cuda(), g.k_cache, g.v_cache, g.block_tables, g.context_lens, qs.cuda(), scale, out,
+                                max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    ref = oracle.attention_prefill(q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, qs, scale)
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 2e-3
+
+
 def test_one_new_token_matches_decode():
     w, q, qs = workloads.prefill_workload(310_950, num_seqs=9, max_len=1500, min_len=1, num_q_heads=32,
                                           num_kv_heads=8, new_tokens=lambda s, L: 1)
