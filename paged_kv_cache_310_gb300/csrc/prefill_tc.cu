@@ -298,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     pcur.init(p.work_list, num_items);
     int pc = 0, pst = 0, pph = 0, pk = 0, pn = qn;
     bool ok = true;
-    // QK of chunk qc for both tiles
-    auto qk_pair = [&]() -> bool {
+    // QK of chunk qc for both tiles (k_seen: its K stage was already seen landed)
+    auto qk_pair = [&](bool k_seen) -> bool {
       const int qj = qcur.k, qb = qj & 1, sb = qc & 1;
       if (qk == 0 && !wait_all(&bars.qfull[qb], (qj >> 1) & 1)) return false;
-      if (!wait_all(&bars.kfull[qst], qph)) return false;
+      if (!k_seen && !wait_all(&bars.kfull[qst], qph)) return false;
       const bool last = qk == qn - 1;
       const uint64_t dk = dk0 + ((qst * kKVTile) >> 4);
       const uint64_t dqb = dq0 + ((qb * kQItem) >> 4);
@@ -335,15 +335,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       }
       return true;
     };
-    for (int i = 0; i < 2 && ok && qcur.valid(); ++i) ok = qk_pair();
+    for (int i = 0; i < 2 && ok && qcur.valid(); ++i) ok = qk_pair(false);
     while (ok && pcur.valid()) {
       const int sb = pc & 1;
-      if (!wait_all(&bars.vfull[pst], pph)) break;
+      static_assert(kGroups == 2, "the probe below covers two tiles");
+      // one round trip probes everything this iteration needs (V of chunk pc, both
+      // tiles' probabilities, K of chunk pc + 2); only what is not ready yet is waited for
+      const uint32_t seen = __shfl_sync(0xffffffffu,
+          mbar_test_wait4(&bars.vfull[pst], pph, bars.pfull(0, sb), (pc >> 1) & 1, bars.pfull(1, sb),
+                          (pc >> 1) & 1, &bars.kfull[qst], qph), 0);
+      if (!(seen & 1) && !wait_all(&bars.vfull[pst], pph)) break;
       const uint64_t dv = dv0 + ((pst * kKVTile) >> 4);
       const bool acc0 = pk > 0;
 #pragma unroll
       for (int g = 0; g < kGroups; ++g) {
-        if (!wait_all(bars.pfull(g, sb), (pc >> 1) & 1)) {
+        if (!(seen & (2u << g)) && !wait_all(bars.pfull(g, sb), (pc >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         pcur.advance();
         pn = pcur.valid() ? unpack_item(pcur.cur, TQ).nchunks : 0;
       }
-      if (qcur.valid()) ok = qk_pair();
+      if (qcur.valid()) ok = qk_pair((seen & 8u) != 0);
     }
     __syncwarp();
   } else {
