@@ -244,8 +244,10 @@ size_t paged_attention_no_alloc_limit(void);
  * query_start: device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0 and
  * query_start[num_seqs] = num_query_tokens.  A sequence with n_s > context_lens[s]
  * or context_lens[s] > max_context_len sets the device index flag and is skipped.
- * Tensor cores only: f16/bf16, head_dim 128, query-head groups <= 16.  workspace:
- * at least paged_attention_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ * Tensor cores only: f16/bf16, head_dim 128, query-head groups <= 16, block size 8,
+ * 16 or 32, at most 4095 KV heads (else PKV_ERR_UNSUPPORTED); q, out and the pools
+ * 16-byte aligned.  workspace: at least paged_attention_prefill_workspace_bytes(...)
+ * bytes, 256-byte aligned.
  */
 size_t paged_attention_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_query_tokens,
                                                const pkv_cache_desc* cache);

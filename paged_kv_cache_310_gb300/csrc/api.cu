@@ -432,7 +432,8 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
   const int group = num_q_heads / cache->num_kv_heads;
   if (!tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
     return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 128 and query-head groups <= 16");
-  if (cache->num_kv_heads > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d", cache->num_kv_heads);
+  if (cache->num_kv_heads > 4095)  // a work-list entry packs the KV head into 12 bits
+    return fail(PKV_ERR_UNSUPPORTED, "prefill supports at most 4095 KV heads (%d)", cache->num_kv_heads);
   if (num_query_tokens < 0 || max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
   if (num_seqs == 0 || num_query_tokens == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)

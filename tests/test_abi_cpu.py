@@ -141,3 +141,29 @@ def test_plan_reports_path_partitions_and_launches(lib):
     assert pkv.paged_attention_plan(64, 8, 2048, k32)["path"] == pkv.PATH_CUDA_CORE   # f32, D64
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_attention_plan(64, 8, 2048, k16, path=pkv.PATH_TENSOR_CORE, partition_tokens=8192)
+
+
+def test_prefill_argument_checks_before_device_work(lib):
+    a = ctypes.c_void_p(0x10000)
+
+    def run(desc, Hq=64, T=100, S=4, L=4096, mbps=256, out_dtype=pkv.BF16, ws=None, wsb=0, q=a, scale=0.1):
+        return lib.paged_attention_prefill(q, a, a, a, mbps, a, a, S, Hq, T, L, scale, a, out_dtype, ws, wsb,
+                                           ctypes.byref(desc), None)
+
+    d = _desc()
+    need = lib.paged_attention_prefill_workspace_bytes(4, 64, 100, ctypes.byref(d))
+    assert need > 256
+    assert run(_desc(dtype=pkv.F32)) == 2                       # f32 has no prefill path
+    assert run(_desc(head_dim=64)) == 2
+    assert run(d, Hq=8 * 17) == 2                               # group 17
+    assert run(_desc(num_kv_heads=4096), Hq=4096) == 2           # KV head packed in 12 bits
+    assert b"4095" in lib.paged_kv_last_error()
+    assert run(d, Hq=60) == 1                                   # not a multiple of the KV heads
+    assert run(d, ws=None) == 3                                 # no workspace
+    assert run(d, ws=ctypes.c_void_p(0x10100), wsb=need - 256) == 3
+    assert run(d, ws=ctypes.c_void_p(0x10080), wsb=need) == 1   # workspace not 256-byte aligned
+    assert run(d, q=ctypes.c_void_p(0x10008), ws=a, wsb=need) == 1  # q not 16-byte aligned
+    assert run(d, mbps=255, ws=a, wsb=need) == 1                # table narrower than max length needs
+    assert run(d, out_dtype=pkv.F16, ws=a, wsb=need) == 2       # out must be the cache dtype or f32
+    assert run(d, scale=float("inf"), ws=a, wsb=need) == 1
+    assert run(d, T=0) == 0 and run(d, S=0) == 0                # nothing to do
