@@ -111,6 +111,29 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with launch_dependent() may start
+// before the previous kernel on the stream has finished; grid_dependency_wait() blocks
+// until that kernel has completed and its memory operations are visible (a no-op for
+// an ordinary launch).  grid_dependents_launch() lets the next such kernel start early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename Kernel, typename Args>
+cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int smem_bytes, cudaStream_t stream,
+                             const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 // Non-blocking probe of the same condition (for a thread polling several barriers).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;

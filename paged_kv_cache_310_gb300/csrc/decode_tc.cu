@@ -143,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // chunks the producer issued
   int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // chunks the MMA lane saw land
   const int G = p.group;
-  const int num_items = *p.work_count;  // written by the work-list kernel earlier on the stream
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -169,6 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched while the work-list kernel may still run (programmatic dependent launch):
+  // everything above touches only this CTA; the list, the pool and q are read after
+  // the preceding kernels on the stream have completed and their writes are visible.
+  grid_dependency_wait();
+  const int num_items = *p.work_count;
 
   if (warp == 4) {
     // ============================ TMA producer ============================
@@ -517,6 +521,7 @@ constexpr int kMaxChunkCounts = kTcMaxPartition / kChunk;
 
 template <typename T>
 __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_constant__ DecodeParams p) {
+  grid_dependents_launch();  // the decode kernel may start its prologue now
   __shared__ int hist[kMaxChunkCounts + 1];
   __shared__ int next[kMaxChunkCounts + 1];
   const int full_chunks = p.part_tokens / kChunk;
@@ -586,8 +591,7 @@ cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  decode_tc_kernel<T, GM><<<grid, kThreads, kSmemBytes, stream>>>(args);
-  return cudaGetLastError();
+  return launch_dependent(decode_tc_kernel<T, GM>, grid, kThreads, kSmemBytes, stream, args);
 }
 
 template <typename T>
