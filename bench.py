@@ -83,6 +83,22 @@ def recorded_traffic(path_name, workload, partition):
     return None
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (the slowest rank sets a whole-job time); x itself
+    when there is no process group."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def whole_job_rate(world, bytes_per_rank, ms):
+    """Bytes per second of all ranks together, in GB/s: every rank moves bytes_per_rank
+    in ms (the max over ranks)."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -366,10 +382,7 @@ def main():
     clk = clocks.stop()
     total_ms = t_begin.elapsed_time(t_end)
     decode_ms = statistics.mean(m.elapsed_time(e) for m, e in zip(mids, ends))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t)
+    total_ms = max_over_ranks(total_ms, dist, dev)
     if pkv.device_error() != 0:
         raise SystemExit("device error flag set in the timed region")
     ms_per_step = total_ms / args.steps
@@ -450,15 +463,12 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / n_e2e
     if not torch.equal(out_host[(n_e2e - 1) % 2], out.cpu()):
         raise SystemExit("end-to-end output differs from the device-timed output")
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     kv_bytes, algo_bytes = roofline_bytes(w, elem(out.dtype))
     peak, peak_kind = peaks()
     tokens = int(w.context_lens.sum())
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(world, kv_bytes, ms_per_step)
     achieved = algo_bytes / (decode_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -479,7 +489,7 @@ def main():
                                                  plan["partition_tokens"]),
                      "kernel": "paged_attention_decode (work list + decode_tc, or decode_simt + merge)",
                      "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": decode_ms},
-        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(world, kv_bytes, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
