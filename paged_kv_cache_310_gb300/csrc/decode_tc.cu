@@ -12,11 +12,15 @@
 // fp32 CUDA-core rate; as two small dense contractions per 128-token chunk it is a
 // few percent of the tensor cores:
 //   S^T[128 tokens x 16] = K[128 x 128 dims] . Q^T[128 x 16]          (QK, M=128 N=16)
-//   O^T[128 dims x 16]   = V^T[128 dims x 128 tokens] . P^T[128 x 16]  (PV, M=128 N=16)
-// The query heads of a group are the N dimension (padded to 16 with unused columns).
+//   O^T[128 dims x N]    = V^T[128 dims x 128 tokens] . P^T[128 x N]   (PV, M=128)
+// The query heads of a group are the N dimension of QK (padded to 16).  PV's columns
+// hold each head's probabilities twice, as a rounded part and its remainder (N = 16
+// up to 8 heads, 32 up to 16).
 //
-// Persistent CTAs (one per SM, static round-robin over work items = (partition,
-// sequence, KV head)), 192 threads in four roles:
+// Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
+// head) that work_list_kernel sorts longest first and the CTAs take in snake order;
+// the kernel is launched as a programmatic dependent of that list kernel.  192 threads
+// in four roles:
 //  * warp 4, producer: per 128-token chunk, one lane per physical block reads the
 //    block id (before waiting for a free stage, hiding its latency) and issues two
 //    tiled TMA loads (the block's K tile and V tile for this KV head, 4-D boxes,
