@@ -32,10 +32,13 @@
  * Conventions:
  *  - Ownership: the caller owns every buffer.  Apart from arguments documented as
  *    host memory, every pointer is device memory of the current device.  The
- *    library allocates no device memory, keeps no pointer after a call returns,
- *    and needs caller-provided workspace only for split-K decode.
+ *    library allocates no device memory and keeps no pointer after a call returns.
+ *    Caller-provided workspace holds the tensor-core decode work list, split-K
+ *    partials and the prefill work list (the *_workspace_bytes calls size it).
  *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *    call only enqueues work and returns; results are ready when the stream is.
+ *    The calls can be captured in a CUDA graph once each kind has run once outside
+ *    the capture (the first call sets its kernels' shared-memory limits).
  *  - Alignment: q, k, v, out, k_cache, v_cache must be 16-byte aligned, and
  *    head_dim * element size must be a multiple of 16 bytes.
  *  - Errors: a call returns PKV_OK or an error status and records a message that
@@ -46,7 +49,9 @@
  *    paged_kv_device_error() reports and clears that flag.
  *  - Supported set: dtype f32, f16, bf16 (q, k, v, caches share it); out dtype
  *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16 or 32;
- *    num_q_heads a multiple of num_kv_heads with group size <= 8.
+ *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
+ *    up to 8 on the CUDA-core decode path and up to 16 on the tensor-core paths
+ *    (f16/bf16, head_dim 128).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -169,9 +174,9 @@ pkv_status paged_block_swap_in(const int64_t* block_ids, int32_t num_ids, const 
  * Bytes of workspace paged_attention_decode needs for these sizes and config.  The
  * CUDA-core path needs none when every sequence fits one partition; the tensor-core
  * path always needs room for its work list (16 bytes per (sequence, KV head,
- * partition) plus 256) and, past one partition, the partition partials.  max_context_len: host upper bound on
- * context_lens.  Returns 0 for invalid arguments as well (then the decode call
- * itself reports the error).
+ * partition) plus 256) and, past one partition, the partition partials.
+ * max_context_len: host upper bound on context_lens.  Returns 0 for invalid
+ * arguments as well (then the decode call itself reports the error).
  */
 size_t paged_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                        int32_t max_context_len, const pkv_cache_desc* cache,
