@@ -78,3 +78,30 @@ def test_one_new_token_matches_decode():
                                max_context_len=w.max_context_len)
     torch.cuda.synchronize()
     assert (out - dec).abs().max().item() <= 2e-3
+
+
+def test_bench_prefill_workload_sampled():
+    """The chunked-prefill workload bench.py times (same seed, sizes and launch): every
+    output computed on the GPU in one call, two whole sequences' outputs checked against
+    the oracle, the rest checked finite."""
+    dev = torch.device("cuda")
+    nq = 512
+    w, q, qs = workloads.prefill_workload(310_990, num_seqs=32, max_len=4096, min_len=1024, num_q_heads=64,
+                                          num_kv_heads=8, block_size=16, dtype="bf16",
+                                          new_tokens=lambda s, L: nq, canary=False, pool_device=dev)
+    g = w.to(dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    pkv.paged_attention_prefill(q.to(dev), g.k_cache, g.v_cache, g.block_tables, g.context_lens, qs.to(dev),
+                                w.scale, out, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    got = out.cpu()
+    assert torch.isfinite(got).all()
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    tables, lens, qh = w.block_tables.cpu(), w.context_lens.cpu(), q.cpu()
+    for s in (0, 17):
+        rows = slice(int(qs[s]), int(qs[s + 1]))
+        ref = oracle.attention_prefill(qh[rows], kc, vc, tables[s:s + 1], lens[s:s + 1],
+                                       torch.tensor([0, nq], dtype=torch.int32), w.scale)
+        err = np.abs(got[rows].double().numpy() - ref).max()
+        assert err <= 2e-3, f"sequence {s}: max-abs {err:.3g}"
