@@ -240,81 +240,93 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ============================
-    // One lane polls both streams and issues whichever is ready: QK of the next chunk
-    // (its K/V landed, its S buffer free) or PV of the oldest chunk whose
-    // probabilities are written.  Neither waits behind the other.
-    if (lane == 0) {
-      constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-      constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
-      constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, GM <= 8 ? 16 : 32);
-      const uint32_t ring = smem_addr(smem);
-      const uint32_t qbase = smem_addr(smem + kOffQ);
-      const uint32_t pbase = smem_addr(smem + kOffP);
-      // QK cursor: items walked, chunk within the item, chunks in the item
-      ItemCursor qcur;
-      qcur.init(p.work_list, num_items);
-      int qk = 0, qj = 0;
-      int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
-      int qc = 0, pc = 0;  // next chunk to QK, next chunk to PV
-      uint64_t idle_since = global_timer_ns();
-      while (qcur.valid() || pc < qc) {
-        bool progressed = false;
-        if (qcur.valid()) {
-          const int st = qc % kStages, sb = qc & 1, qb = qj & 1;
-          if ((qk > 0 || mbar_try_wait(&bars.qfull[qb], (qj >> 1) & 1)) &&
-              mbar_try_wait(&bars.full[st], (qc / kStages) & 1) &&
-              (qc < 2 || mbar_try_wait(&bars.sfree[sb], ((qc >> 1) - 1) & 1))) {
-            *waited_slot = qc + 1;
-            tc_fence_after();
-            const uint32_t kb = ring + st * kStageBytes;
-            const uint32_t qa = qbase + qb * kQBytes;
+    // The whole warp polls with warp-uniform control flow (descriptors and counters
+    // stay in uniform registers) and one elected lane issues whichever is ready: QK of
+    // the next chunk (its K/V landed, its S buffer free) or PV of the oldest chunk whose
+    // probabilities are written.  Neither waits behind the other.  One round trip
+    // probes the four barriers both need.
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
+    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, GM <= 8 ? 16 : 32);
+    // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
+    const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroupBytes, kLayoutSwizzle128);
+    const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, 1024, kLayoutSwizzle128);
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kTileBytes), 1024, kGroupBytes, kLayoutSwizzle128);
+    const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, kChunk * 16, kLayoutNone);
+    // QK cursor: items walked, chunk within the item, chunks in the item
+    ItemCursor qcur;
+    qcur.init(p.work_list, num_items);
+    int qk = 0, qj = 0;
+    int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+    int qc = 0, pc = 0;           // next chunk to QK, next chunk to PV
+    int qst = 0, qph = 0;         // ring stage and phase of chunk qc
+    int pst = 0;                  // ring stage of chunk pc
+    uint64_t idle_since = global_timer_ns();
+    while (qcur.valid() || pc < qc) {
+      bool progressed = false;
+      const int sb = qc & 1, qb = qj & 1, pb = pc & 1;
+      // bit 0: chunk qc landed, 1: S[qc & 1] free, 2: P of chunk pc written, 3: O[pc & 1] free
+      const uint32_t seen = __shfl_sync(0xffffffffu,
+          mbar_test_wait4(&bars.full[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
+                          (pc >> 1) & 1, &bars.ofree[pb], ((pc >> 1) - 1) & 1), 0);
+      if (qcur.valid() && (seen & 1) && (qc < 2 || (seen & 2)) &&
+          (qk > 0 || __all_sync(0xffffffffu, mbar_test_wait(&bars.qfull[qb], (qj >> 1) & 1)))) {
+        *waited_slot = qc + 1;
+        const uint64_t dk = dk0 + ((qst * kStageBytes) >> 4);
+        const uint64_t dq = dq0 + ((qb * kQBytes) >> 4);
+        const bool last = qk == qn - 1;
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = smem_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kGroupBytes,
-                                            kLayoutSwizzle128);
-              const uint64_t bd = smem_desc(qa + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024,
-                                            kLayoutSwizzle128);
-              mma_f16(tmem + sb * 16, ad, bd, idesc_qk, kk > 0);
-            }
-            mma_commit(&bars.sfull[sb]);
-            ++qc;
-            if (++qk == qn) {  // the item's last QK: its query buffer can be refilled
-              mma_commit(&bars.qempty[qb]);
-              qk = 0;
-              ++qj;
-              qcur.advance();
-              qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
-            }
-            progressed = true;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ko = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            const uint32_t qo = ((kk >> 2) * (kQBytes / 2) + (kk & 3) * 32) >> 4;
+            mma_f16(tmem + sb * 16, dk + ko, dq + qo, idesc_qk, kk > 0);
           }
+          mma_commit(&bars.sfull[sb]);
+          if (last) mma_commit(&bars.qempty[qb]);  // the item's last QK: its query buffer can be refilled
         }
-        if (pc < qc) {
-          const int pb = pc & 1, st = pc % kStages;
-          if (mbar_try_wait(&bars.pfull[pb], (pc >> 1) & 1) &&
-              (pc < 2 || mbar_try_wait(&bars.ofree[pb], ((pc >> 1) - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t vbase = ring + st * kStageBytes + kTileBytes;
+        __syncwarp();
+        ++qc;
+        if (++qst == kStages) {
+          qst = 0;
+          qph ^= 1;
+        }
+        if (++qk == qn) {
+          qk = 0;
+          ++qj;
+          qcur.advance();
+          qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+        }
+        progressed = true;
+      }
+      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8))) {
+        const uint64_t dv = dv0 + ((pst * kStageBytes) >> 4);
+        const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kChunk / 16; ++kk) {
-              const uint64_t ad = smem_desc(vbase + kk * 2 * kGroupBytes, 1024, kGroupBytes, kLayoutSwizzle128);
-              const uint64_t bd = smem_desc(pbase + pb * kPBytes + kk * 256, 128, kChunk * 16, kLayoutNone);
-              mma_f16(tmem + 32 + pb * 32, ad, bd, idesc_pv, kk > 0);
-            }
-            mma_commit(&bars.ofull[pb]);
-            mma_commit(&bars.empty[st]);
-            ++pc;
-            progressed = true;
-          }
+          for (int kk = 0; kk < kChunk / 16; ++kk)
+            mma_f16(tmem + 32 + pb * 32, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
+                    kk > 0);
+          mma_commit(&bars.ofull[pb]);
+          mma_commit(&bars.empty[pst]);
         }
-        if (progressed) {
-          idle_since = global_timer_ns();
-        } else {
-          if (*abort_flag) break;
-          if (global_timer_ns() - idle_since > kWaitLimitNs) {
+        __syncwarp();
+        ++pc;
+        if (++pst == kStages) pst = 0;
+        progressed = true;
+      }
+      if (progressed) {
+        idle_since = global_timer_ns();
+      } else {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        if (__any_sync(0xffffffffu, global_timer_ns() - idle_since > kWaitLimitNs)) {
+          if (lane == 0) {
             *abort_flag = 1;
             set_error(p.err, kErrTimeout);
-            break;
           }
+          break;
         }
       }
     }
