@@ -51,7 +51,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                  // 4 softmax warps, K producer, MMA, V producer
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
 constexpr int kStages = 3;
 constexpr int kN = 16;                         // MMA N: query heads per group, padded
@@ -62,7 +62,6 @@ constexpr int kN = 16;                         // MMA N: query heads per group, 
 // apart, 64-dimension blocks 1 KB apart), and one 4-D TMA box fills a whole block.
 constexpr int kGroupBytes = 2048;               // one 8-row group: both halves
 constexpr int kTileBytes = kChunk * 256;        // K or V of one chunk: 32 KB
-constexpr int kStageBytes = 2 * kTileBytes;     // K then V
 constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 128 B
 // P^T holds each probability as two rounded parts, hi = round(p) and
 // lo = round(p - hi), as separate groups of 8 columns: the PV MMA then sums
@@ -70,10 +69,13 @@ constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 
 // 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (N = 16, the columns are there anyway);
 // up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (N = 32).
 constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
-constexpr int kOffQ = kStages * kStageBytes;
+// K and V have separate rings: a K stage is free once the chunk's QK completed, long
+// before its V (needed until PV completes), so more of the rings stays in flight.
+constexpr int kOffV = kStages * kTileBytes;
+constexpr int kOffQ = 2 * kStages * kTileBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 2 * kStages + 7 * 2 + 1;  // ring (full, empty), 7 pairs, drain
+constexpr int kNumBars = 4 * kStages + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
 constexpr int kOffRedMax = kOffBar + kNumBars * 8;
 constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
 constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
@@ -81,8 +83,10 @@ constexpr int kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
 struct Bars {
-  uint64_t* full;   // [kStages] K/V chunk landed (TMA tx)
-  uint64_t* empty;  // [kStages] chunk's MMAs done
+  uint64_t* kfull;  // [kStages] K of a chunk landed (TMA tx)
+  uint64_t* kempty; // [kStages] the chunk's QK done
+  uint64_t* vfull;  // [kStages] V of a chunk landed
+  uint64_t* vempty; // [kStages] the chunk's PV done
   uint64_t* qfull;  // [2] query tile landed
   uint64_t* qempty; // [2] QK MMAs of that item done
   uint64_t* sfull;  // [2] S ready
@@ -96,9 +100,11 @@ struct Bars {
 __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
   Bars r;
-  r.full = b;
-  r.empty = b + kStages;
-  r.qfull = b + 2 * kStages;
+  r.kfull = b;
+  r.kempty = b + kStages;
+  r.vfull = b + 2 * kStages;
+  r.vempty = b + 3 * kStages;
+  r.qfull = b + 4 * kStages;
   r.qempty = r.qfull + 2;
   r.sfull = r.qempty + 2;
   r.sfree = r.sfull + 2;
@@ -144,14 +150,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   float* red_l = reinterpret_cast<float*>(smem + kOffRedL);      // [4 warps][kN]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* issued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // chunks the producer issued
-  int* waited_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // chunks the MMA lane saw land
+  int* kissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // K chunks issued
+  int* vissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // V chunks issued
   const int G = p.group;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], 1);
+      mbar_init(&bars.kfull[i], 1);
+      mbar_init(&bars.kempty[i], 1);
+      mbar_init(&bars.vfull[i], 1);
+      mbar_init(&bars.vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.qfull[i], 1);
@@ -163,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_init(&bars.ofree[i], 4);
     }
     *abort_flag = 0;
-    *issued_slot = 0;
-    *waited_slot = 0;
+    *kissued_slot = 0;
+    *vissued_slot = 0;
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
@@ -215,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
-          ok = c < kStages || wait_role(&bars.empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
-          if (ok) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
+          ok = c < kStages || wait_role(&bars.kempty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -230,13 +238,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             row = (b * p.num_kv_heads + it.g) * bs;
           }
-          unsigned char* dst = smem + st * kStageBytes + lane * bs * 256;
-          tma_load_4d(dst, &a.tk, row / 8, &bars.full[st], pol_stream);
-          tma_load_4d(dst + kTileBytes, &a.tv, row / 8, &bars.full[st], pol_stream);
+          tma_load_4d(smem + st * kTileBytes + lane * bs * 256, &a.tk, row / 8, &bars.kfull[st], pol_stream);
         }
-        if (lane == 0) *issued_slot = c + 1;
+        if (lane == 0) *kissued_slot = c + 1;
       }
       ++j;
+    }
+  } else if (warp == 6) {
+    // ============================ TMA producer of V ============================
+    if (lane == 0) prefetch_tensormap(&a.tv);
+    const uint64_t pol_stream = policy_evict_first();
+    const int bs = p.block_size;
+    const int blocks_per_chunk = kChunk / bs;
+    const int oob_row = p.num_blocks * p.num_kv_heads * bs;
+    int c = 0;
+    bool ok = true;
+    ItemCursor cur;
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+      const Item it = unpack_item(cur.cur, p.part_tokens);
+      const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
+      for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
+        const int st = c % kStages;
+        const int lb = it.t0 / bs + k * blocks_per_chunk + lane;
+        const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
+        int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
+        if (lane == 0) {
+          ok = c < kStages || wait_role(&bars.vempty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+          if (ok) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        __syncwarp();
+        if (lane < blocks_per_chunk) {
+          int row = oob_row;
+          if (live) {
+            if (b < 0 || b >= p.num_blocks) b = 0;  // the K producer flags it
+            row = (b * p.num_kv_heads + it.g) * bs;
+          }
+          tma_load_4d(smem + kOffV + st * kTileBytes + lane * bs * 256, &a.tv, row / 8, &bars.vfull[st], pol_stream);
+        }
+        if (lane == 0) *vissued_slot = c + 1;
+      }
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ============================
@@ -251,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
     const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroupBytes, kLayoutSwizzle128);
     const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, 1024, kLayoutSwizzle128);
-    const uint64_t dv0 = smem_desc(smem_addr(smem + kTileBytes), 1024, kGroupBytes, kLayoutSwizzle128);
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), 1024, kGroupBytes, kLayoutSwizzle128);
     const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, kChunk * 16, kLayoutNone);
     // QK cursor: items walked, chunk within the item, chunks in the item
     ItemCursor qcur;
@@ -260,19 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
     int qc = 0, pc = 0;           // next chunk to QK, next chunk to PV
     int qst = 0, qph = 0;         // ring stage and phase of chunk qc
-    int pst = 0;                  // ring stage of chunk pc
+    int pst = 0, pph = 0;         // ring stage and phase of chunk pc
     uint64_t idle_since = global_timer_ns();
     while (qcur.valid() || pc < qc) {
       bool progressed = false;
       const int sb = qc & 1, qb = qj & 1, pb = pc & 1;
       // bit 0: chunk qc landed, 1: S[qc & 1] free, 2: P of chunk pc written, 3: O[pc & 1] free
       const uint32_t seen = __shfl_sync(0xffffffffu,
-          mbar_test_wait4(&bars.full[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
+          mbar_test_wait4(&bars.kfull[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
                           (pc >> 1) & 1, &bars.ofree[pb], ((pc >> 1) - 1) & 1), 0);
       if (qcur.valid() && (seen & 1) && (qc < 2 || (seen & 2)) &&
           (qk > 0 || __all_sync(0xffffffffu, mbar_test_wait(&bars.qfull[qb], (qj >> 1) & 1)))) {
-        *waited_slot = qc + 1;
-        const uint64_t dk = dk0 + ((qst * kStageBytes) >> 4);
+        const uint64_t dk = dk0 + ((qst * kTileBytes) >> 4);
         const uint64_t dq = dq0 + ((qb * kQBytes) >> 4);
         const bool last = qk == qn - 1;
         tc_fence_after();
@@ -284,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             mma_f16(tmem + sb * 16, dk + ko, dq + qo, idesc_qk, kk > 0);
           }
           mma_commit(&bars.sfull[sb]);
+          mma_commit(&bars.kempty[qst]);           // the K stage is free once this QK completed
           if (last) mma_commit(&bars.qempty[qb]);  // the item's last QK: its query buffer can be refilled
         }
         __syncwarp();
@@ -300,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         progressed = true;
       }
-      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8))) {
-        const uint64_t dv = dv0 + ((pst * kStageBytes) >> 4);
+      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8)) &&
+          __all_sync(0xffffffffu, mbar_test_wait(&bars.vfull[pst], pph))) {
+        const uint64_t dv = dv0 + ((pst * kTileBytes) >> 4);
         const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
         tc_fence_after();
         if (elect_one()) {
@@ -310,11 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             mma_f16(tmem + 32 + pb * 32, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
                     kk > 0);
           mma_commit(&bars.ofull[pb]);
-          mma_commit(&bars.empty[pst]);
+          mma_commit(&bars.vempty[pst]);
         }
         __syncwarp();
         ++pc;
-        if (++pst == kStages) pst = 0;
+        if (++pst == kStages) {
+          pst = 0;
+          pph ^= 1;
+        }
         progressed = true;
       }
       if (progressed) {
@@ -455,9 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         // rows of the last loaded block past the context end: zero their V rows
         const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
-        if (t >= rows_valid && t < rows_loaded) {
-          unsigned char* vrow = smem + (c % kStages) * kStageBytes + kTileBytes + (t >> 3) * kGroupBytes +
-                                (t & 7) * 128;
+        // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
+        const bool v_ok = rows_valid >= rows_loaded ||
+                          __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kStages], (c / kStages) & 1, abort_flag, p.err));
+        if (v_ok && t >= rows_valid && t < rows_loaded) {
+          unsigned char* vrow = smem + kOffV + (c % kStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
@@ -510,9 +558,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   __syncthreads();
   if (*abort_flag) {
     // a wait ran out: let in-flight copies and MMAs finish (bounded) before leaving
+    // copies still in flight land first: the last chunk issued on each stage (a
+    // phase already completed returns at once)
     if (warp == 4 && lane == 0) {
-      for (int c = *waited_slot; c < *issued_slot; ++c)
-        if (!mbar_wait(&bars.full[c % kStages], (c / kStages) & 1)) break;
+      for (int c = max(0, *kissued_slot - kStages); c < *kissued_slot; ++c)
+        if (!mbar_wait(&bars.kfull[c % kStages], (c / kStages) & 1)) break;
+    }
+    if (warp == 6 && lane == 0) {
+      for (int c = max(0, *vissued_slot - kStages); c < *vissued_slot; ++c)
+        if (!mbar_wait(&bars.vfull[c % kStages], (c / kStages) & 1)) break;
     }
     if (warp == 5 && lane == 0) {
       mbar_init(bars.drain, 1);
