@@ -283,10 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   } else if (warp == 5) {
     // ============================ MMA issuer ============================
     // The whole warp polls with warp-uniform control flow (descriptors and counters
-    // stay in uniform registers) and one elected lane issues whichever is ready: QK of
-    // the next chunk (its K/V landed, its S buffer free) or PV of the oldest chunk whose
-    // probabilities are written.  Neither waits behind the other.  One round trip
-    // probes the four barriers both need.
+    // stay in uniform registers) and one elected lane issues whichever is ready: PV of
+    // the oldest chunk whose probabilities are written (first: its completion frees a
+    // V stage) or QK of the next chunk (its K landed, its S buffer free).  Neither waits
+    // behind the other.  One round trip probes the four barriers both need.
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
     constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, GM <= 8 ? 16 : 32);
@@ -311,6 +311,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const uint32_t seen = __shfl_sync(0xffffffffu,
           mbar_test_wait4(&bars.kfull[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
                           (pc >> 1) & 1, &bars.ofree[pb], ((pc >> 1) - 1) & 1), 0);
+      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8)) &&
+          __all_sync(0xffffffffu, mbar_test_wait(&bars.vfull[pst], pph))) {
+        const uint64_t dv = dv0 + ((pst * kTileBytes) >> 4);
+        const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kChunk / 16; ++kk)
+            mma_f16(tmem + 32 + pb * 32, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
+                    kk > 0);
+          mma_commit(&bars.ofull[pb]);
+          mma_commit(&bars.vempty[pst]);
+        }
+        __syncwarp();
+        ++pc;
+        if (++pst == kStages) {
+          pst = 0;
+          pph ^= 1;
+        }
+        progressed = true;
+      }
       if (qcur.valid() && (seen & 1) && (qc < 2 || (seen & 2)) &&
           (qk > 0 || __all_sync(0xffffffffu, mbar_test_wait(&bars.qfull[qb], (qj >> 1) & 1)))) {
         const uint64_t dk = dk0 + ((qst * kTileBytes) >> 4);
@@ -339,27 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           ++qj;
           qcur.advance();
           qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
-        }
-        progressed = true;
-      }
-      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8)) &&
-          __all_sync(0xffffffffu, mbar_test_wait(&bars.vfull[pst], pph))) {
-        const uint64_t dv = dv0 + ((pst * kTileBytes) >> 4);
-        const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
-        tc_fence_after();
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk)
-            mma_f16(tmem + 32 + pb * 32, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
-                    kk > 0);
-          mma_commit(&bars.ofull[pb]);
-          mma_commit(&bars.vempty[pst]);
-        }
-        __syncwarp();
-        ++pc;
-        if (++pst == kStages) {
-          pst = 0;
-          pph ^= 1;
         }
         progressed = true;
       }
