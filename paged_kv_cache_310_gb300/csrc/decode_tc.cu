@@ -53,7 +53,8 @@ namespace {
 
 constexpr int kThreads = 224;                  // 4 softmax warps, K producer, MMA, V producer
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
-constexpr int kStages = 3;
+constexpr int kKStages = 3;                    // K ring
+constexpr int kVStages = 3;                    // V ring
 constexpr int kN = 16;                         // MMA N: query heads per group, padded
 // A chunk's K (and V) sits in shared memory as [8-row group][64-column half][8 rows]
 // of 128-byte rows: 16 groups x 2 halves x 1 KB = 32 KB, 128-byte swizzled.  That is
@@ -71,11 +72,11 @@ constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 
 constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
 // K and V have separate rings: a K stage is free once the chunk's QK completed, long
 // before its V (needed until PV completes), so more of the rings stays in flight.
-constexpr int kOffV = kStages * kTileBytes;
-constexpr int kOffQ = 2 * kStages * kTileBytes;
+constexpr int kOffV = kKStages * kTileBytes;
+constexpr int kOffQ = (kKStages + kVStages) * kTileBytes;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 4 * kStages + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
+constexpr int kNumBars = 2 * (kKStages + kVStages) + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
 constexpr int kOffRedMax = kOffBar + kNumBars * 8;
 constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
 constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
@@ -83,10 +84,10 @@ constexpr int kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
 struct Bars {
-  uint64_t* kfull;  // [kStages] K of a chunk landed (TMA tx)
-  uint64_t* kempty; // [kStages] the chunk's QK done
-  uint64_t* vfull;  // [kStages] V of a chunk landed
-  uint64_t* vempty; // [kStages] the chunk's PV done
+  uint64_t* kfull;  // [kKStages] K of a chunk landed (TMA tx)
+  uint64_t* kempty; // [kKStages] the chunk's QK done
+  uint64_t* vfull;  // [kVStages] V of a chunk landed
+  uint64_t* vempty; // [kVStages] the chunk's PV done
   uint64_t* qfull;  // [2] query tile landed
   uint64_t* qempty; // [2] QK MMAs of that item done
   uint64_t* sfull;  // [2] S ready
@@ -101,10 +102,10 @@ __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
   Bars r;
   r.kfull = b;
-  r.kempty = b + kStages;
-  r.vfull = b + 2 * kStages;
-  r.vempty = b + 3 * kStages;
-  r.qfull = b + 4 * kStages;
+  r.kempty = b + kKStages;
+  r.vfull = b + 2 * kKStages;
+  r.vempty = b + 2 * kKStages + kVStages;
+  r.qfull = b + 2 * (kKStages + kVStages);
   r.qempty = r.qfull + 2;
   r.sfull = r.qempty + 2;
   r.sfree = r.sfull + 2;
@@ -155,9 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int G = p.group;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars.kfull[i], 1);
       mbar_init(&bars.kempty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bars.vfull[i], 1);
       mbar_init(&bars.vempty[i], 1);
     }
@@ -217,13 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       ok = __shfl_sync(0xffffffffu, ok, 0);
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
-        const int st = c % kStages;
+        const int st = c % kKStages;
         // block ids first: their latency overlaps the wait for a free stage
         const int lb = it.t0 / bs + k * blocks_per_chunk + lane;  // logical block of this lane
         const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
-          ok = c < kStages || wait_role(&bars.kempty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+          ok = c < kKStages || wait_role(&bars.kempty[st], ((c / kKStages) - 1) & 1, abort_flag, p.err);
           if (ok) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -258,12 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const Item it = unpack_item(cur.cur, p.part_tokens);
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
-        const int st = c % kStages;
+        const int st = c % kVStages;
         const int lb = it.t0 / bs + k * blocks_per_chunk + lane;
         const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
-          ok = c < kStages || wait_role(&bars.vempty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+          ok = c < kVStages || wait_role(&bars.vempty[st], ((c / kVStages) - 1) & 1, abort_flag, p.err);
           if (ok) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         __syncwarp();
         ++pc;
-        if (++pst == kStages) {
+        if (++pst == kVStages) {
           pst = 0;
           pph ^= 1;
         }
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         __syncwarp();
         ++qc;
-        if (++qst == kStages) {
+        if (++qst == kKStages) {
           qst = 0;
           qph ^= 1;
         }
@@ -503,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
         // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
         const bool v_ok = rows_valid >= rows_loaded ||
-                          __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kStages], (c / kStages) & 1, abort_flag, p.err));
+                          __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kVStages], (c / kVStages) & 1, abort_flag, p.err));
         if (v_ok && t >= rows_valid && t < rows_loaded) {
-          unsigned char* vrow = smem + kOffV + (c % kStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
+          unsigned char* vrow = smem + kOffV + (c % kVStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
@@ -561,12 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // copies still in flight land first: the last chunk issued on each stage (a
     // phase already completed returns at once)
     if (warp == 4 && lane == 0) {
-      for (int c = max(0, *kissued_slot - kStages); c < *kissued_slot; ++c)
-        if (!mbar_wait(&bars.kfull[c % kStages], (c / kStages) & 1)) break;
+      for (int c = max(0, *kissued_slot - kKStages); c < *kissued_slot; ++c)
+        if (!mbar_wait(&bars.kfull[c % kKStages], (c / kKStages) & 1)) break;
     }
     if (warp == 6 && lane == 0) {
-      for (int c = max(0, *vissued_slot - kStages); c < *vissued_slot; ++c)
-        if (!mbar_wait(&bars.vfull[c % kStages], (c / kStages) & 1)) break;
+      for (int c = max(0, *vissued_slot - kVStages); c < *vissued_slot; ++c)
+        if (!mbar_wait(&bars.vfull[c % kVStages], (c / kVStages) & 1)) break;
     }
     if (warp == 5 && lane == 0) {
       mbar_init(bars.drain, 1);
