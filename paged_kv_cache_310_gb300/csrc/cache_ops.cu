@@ -26,6 +26,10 @@ append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
               const int64_t* __restrict__ slots, int32_t num_tokens, uint4* __restrict__ kc,
               uint4* __restrict__ vc, int32_t num_kv_heads, int32_t block_size,
               int32_t row_vecs, int64_t num_slots, int* err) {
+  // A kernel launched after this one as a programmatic dependent (the decode work
+  // list, which reads only context lengths) may start now; it waits for this kernel
+  // before it completes.
+  grid_dependents_launch();
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * row_vecs;
   const int64_t total = per_token * num_tokens;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;

@@ -639,6 +639,10 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
     if (p.context_lens[s] != 0) continue;
     for (int i = lane; i < row; i += 32) store_out<T>(p.out, static_cast<size_t>(s) * row + i, 0.f, p.out_f32);
   }
+  // Launched as a programmatic dependent of the previous kernel (the append, whose
+  // writes this kernel does not read): finish only after it, so the decode kernel's
+  // wait on this one also covers the append.
+  grid_dependency_wait();
 }
 
 // 2-D map over rows of 128 16-bit elements, box 64 x box_rows, 128-byte swizzle.
@@ -697,11 +701,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = items < sms ? items : sms;
-  if (bf16)
-    work_list_kernel<__nv_bfloat16><<<1, kListThreads, 0, stream>>>(p);
-  else
-    work_list_kernel<__half><<<1, kListThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = bf16 ? launch_dependent(work_list_kernel<__nv_bfloat16>, 1, kListThreads, 0, stream, p)
+                       : launch_dependent(work_list_kernel<__half>, 1, kListThreads, 0, stream, p);
   if (e != cudaSuccess || grid == 0) return e;
   return bf16 ? launch_tc_g<__nv_bfloat16>(args, grid, stream) : launch_tc_g<__half>(args, grid, stream);
 }
