@@ -19,18 +19,22 @@
 //
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
 // head) that work_list_kernel sorts longest first and the CTAs take in snake order;
-// the kernel is launched as a programmatic dependent of that list kernel.  192 threads
-// in four roles:
-//  * warp 4, producer: per 128-token chunk, one lane per physical block reads the
-//    block id (before waiting for a free stage, hiding its latency) and issues two
-//    tiled TMA loads (the block's K tile and V tile for this KV head, 4-D boxes,
-//    128-byte swizzle) into a 3-stage ring; blocks past the item's end are loaded
+// the kernel is launched as a programmatic dependent of that list kernel.  224 threads
+// in five roles:
+//  * warp 4, producer of Q and K: per 128-token chunk, one lane per physical block
+//    reads the block id (before waiting for a free stage, hiding its latency) and
+//    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
+//    128-byte swizzle) into a 3-stage K ring; blocks past the item's end are loaded
 //    from outside the tensor, which the TMA unit fills with zeros.  It also loads the
 //    item's 16 query rows.
-//  * warp 5, MMA: one lane polls and issues QK for chunk c into S[c%2] (TMEM) as
-//    soon as its K/V landed, and PV for chunk c into O[c%2] as soon as its
-//    probabilities are in shared memory; commits release the ring stage and signal
-//    the softmax warps.
+//  * warp 6, producer of V: the same for V tiles into a 3-stage V ring.  The rings are
+//    separate so that a K stage is reused as soon as its chunk's QK completes, long
+//    before the chunk's V is done with: more of the rings stays in flight, and the
+//    kernel is bound by bytes in flight.
+//  * warp 5, MMA: the whole warp polls (one batched barrier probe per round) and an
+//    elected lane issues PV for the oldest chunk whose probabilities are in shared
+//    memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed; commits
+//    release the ring stages and signal the softmax warps.
 //  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
 //    chunk max across the 128 tokens (shuffles + shared memory), online-softmax
 //    rescale, probabilities split into two parts rounded to the cache dtype
