@@ -275,9 +275,89 @@ def run_prefill(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / steps
+    if pkv.device_error() != 0:
+        raise SystemExit("device error flag set in the timed region")
     lens = w.context_lens.tolist()
     Hq, D = w.num_q_heads, w.head_dim
     flops = sum(4 * Hq * D * (L - nq + i + 1) for L in lens for i in range(nq))
+
+    # End to end: each step's queries (and query_start) go up from pinned host memory and
+    # its output comes back, on their own streams, double-buffered so that step i's
+    # upload and step i - 1's download overlap the kernels (every copy in the timed region).
+    q_host = q.contiguous().pin_memory()
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    qs_host = qs.contiguous().pin_memory()
+    q_dev = [torch.empty_like(qd) for _ in range(2)]
+    qs_dev = [torch.empty_like(qsd) for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_e2e = max(3, min(args.e2e_steps, 100))
+
+    def e2e_run(n):
+        uploaded, consumed, fetched = [None, None], [None, None], [None, None]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        up.wait_event(t0)
+
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if consumed[b] is not None:
+                    up.wait_event(consumed[b])
+                q_dev[b].copy_(q_host, non_blocking=True)
+                qs_dev[b].copy_(qs_host, non_blocking=True)
+                uploaded[b] = torch.cuda.Event()
+                uploaded[b].record(up)
+
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(uploaded[b])
+            if fetched[b] is not None:
+                stream.wait_event(fetched[b])
+            pkv.paged_attention_prefill(q_dev[b], g.k_cache, g.v_cache, g.block_tables, g.context_lens, qs_dev[b],
+                                        w.scale, outs[b], max_context_len=w.max_context_len)
+            consumed[b] = torch.cuda.Event()
+            consumed[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(consumed[b])
+                out_host[b].copy_(outs[b], non_blocking=True)
+                fetched[b] = torch.cuda.Event()
+                fetched[b].record(down)
+        for f in fetched:
+            if f is not None:
+                stream.wait_event(f)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t1.record(stream)
+        return t0, t1
+
+    e2e_run(2)
+    torch.cuda.synchronize()
+    t0, t1 = e2e_run(n_e2e)
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / n_e2e
+    if not torch.equal(out_host[(n_e2e - 1) % 2], out.cpu()):
+        raise SystemExit("end-to-end output differs from the device-timed output")
+    h2d = q_host.numel() * q_host.element_size() + qs_host.numel() * qs_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
+
+    # CPU baseline: the float64 oracle on one sequence's new tokens, timed on the host cores
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+        tables, lh = w.block_tables.cpu(), w.context_lens.cpu()
+        rows = slice(int(qs[0]), int(qs[1]))
+        t_start = time.perf_counter()
+        oracle.attention_prefill(q[rows], kc, vc, tables[0:1], lh[0:1], torch.tensor([0, nq], dtype=torch.int32),
+                                 w.scale)
+        dt = time.perf_counter() - t_start
+        f0 = sum(4 * Hq * D * (lens[0] - nq + i + 1) for i in range(nq))
+        cpu = {"value": f0 / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"1 of {len(lens)} sequences ({nq} new tokens, context {lens[0]}), one call",
+               "seconds_per_call": dt}
     kv = sum(lens) * 2 * w.num_kv_heads * D * 2
     qo = 2 * int(qs[-1]) * Hq * D * 2
     try:
@@ -299,7 +379,11 @@ def run_prefill(args):
                          "algorithmic_flops_per_launch": flops},
             "hbm": {"algorithmic_bytes_per_launch": kv + qo, "achieved_gbs": (kv + qo) / (ms * 1e-3) / 1e9,
                     "peak": hpeak, "peak_source": hkind},
-            "gpu_launches": 2 * steps, "clocks": clk}
+            "gpu_launches": 2 * steps, "clocks": clk,
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
 
 
