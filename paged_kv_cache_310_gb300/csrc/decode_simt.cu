@@ -12,8 +12,8 @@
 //
 // Inside a CTA:
 //  * warp 4 is the producer: it stages the partition's block ids in shared memory,
-//    then one lane streams the partition through a 4-stage ring.  A stage holds 32
-//    tokens: one 1-D bulk copy (TMA engine, cp.async.bulk) per (block, kv head) tile
+//    then one lane streams the partition through a 3- or 4-stage ring.  A stage holds
+//    32 tokens: one 1-D bulk copy (TMA engine, cp.async.bulk) per (block, kv head) tile
 //    for K and one for V; each tile is block_size*head_dim contiguous elements.
 //    Completion is counted in bytes on the stage's "full" mbarrier.
 //  * warps 0-3 consume.  A row of head_dim elements is spread over head_dim/vec lanes
@@ -30,6 +30,7 @@
 //  combines them: M = max_p m_p, out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
 #include <climits>
 
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -38,8 +39,6 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kChunk = 32;  // tokens per pipeline stage
-constexpr int kStages = 4;
 
 template <typename T, int D, int GM>
 struct Simt {
@@ -47,9 +46,14 @@ struct Simt {
   static constexpr int kLanesPerRow = D / kVec;        // lanes covering one token row
   static constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   static constexpr int kSlots = kConsumerWarps * kRowsPerWarp;
-  static constexpr int kRowsPerSlot = kChunk / kSlots;  // rows a slot handles per stage
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
+  static constexpr int kChunk = 32;                    // tokens per pipeline stage
+  static constexpr int kRowsPerSlot = kChunk / kSlots;  // rows a slot handles per stage
   static constexpr int kStageBytes = 2 * kChunk * kRowBytes;  // K rows then V rows
+  // Four stages, or three of 32 KB (f32, head_dim 128): a 128 KB ring left room for one
+  // CTA per SM, whose prologue and tail then idled the SM (0.74 of copy bandwidth on a
+  // 64 x 32-head batch; 1.04 with two CTAs of three stages).
+  static constexpr int kStages = kStageBytes >= 32768 ? 3 : 4;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kReduceBytes = kSlots * GM * (D + 2) * 4;
   static constexpr int kMainBytes =
@@ -95,17 +99,17 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   const int t0 = part * p.part_tokens;
   if (t0 >= L) return;
   const int ntok = min(p.part_tokens, L - t0);
-  const int nchunks = (ntok + kChunk - 1) / kChunk;
+  const int nchunks = (ntok + C::kChunk - 1) / C::kChunk;
   const int nparts = (L + p.part_tokens - 1) / p.part_tokens;
 
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kMainBytes);
-  uint64_t* empty = full + kStages;
-  int* flags = reinterpret_cast<int*>(empty + kStages);  // [0] first aborted chunk, [1] issued
+  uint64_t* empty = full + C::kStages;
+  int* flags = reinterpret_cast<int*>(empty + C::kStages);  // [0] first aborted chunk, [1] issued
   int* ids = flags + 4;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
@@ -139,21 +143,21 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
       const size_t tile_elems = static_cast<size_t>(bs) * D;
       const size_t block_stride = static_cast<size_t>(p.num_kv_heads) * tile_elems;
       const uint32_t tile_bytes = static_cast<uint32_t>(bs) * C::kRowBytes;
-      const int blocks_per_chunk = kChunk / bs;
+      const int blocks_per_chunk = C::kChunk / bs;
       const uint64_t policy = policy_evict_first();  // K/V are streamed once
       int issued = 0;
       for (int c = 0; c < nchunks; ++c) {
-        const int st = c % kStages;
-        if (c >= kStages && !mbar_wait(&empty[st], ((c / kStages) - 1) & 1)) {
+        const int st = c % C::kStages;
+        if (c >= C::kStages && !mbar_wait(&empty[st], ((c / C::kStages) - 1) & 1)) {
           set_error(p.err, kErrTimeout);
           atomicMin(&flags[0], c);
           break;
         }
         if (*reinterpret_cast<volatile int*>(&flags[0]) != INT_MAX) break;
-        const int rows = min(kChunk, ntok - c * kChunk);
+        const int rows = min(C::kChunk, ntok - c * C::kChunk);
         const int nb = (rows + bs - 1) / bs;
         unsigned char* kdst = ring + st * C::kStageBytes;
-        unsigned char* vdst = kdst + kChunk * C::kRowBytes;
+        unsigned char* vdst = kdst + C::kChunk * C::kRowBytes;
         mbar_arrive_expect_tx(&full[st], 2u * nb * tile_bytes);
         for (int i = 0; i < nb; ++i) {
           const size_t off = ids[c * blocks_per_chunk + i] * block_stride + g * tile_elems;
@@ -188,9 +192,9 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     }
 
     for (int c = 0; c < nchunks; ++c) {
-      const int st = c % kStages;
+      const int st = c % C::kStages;
       // warp-uniform: every lane must take the same branch before the shuffles below
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / C::kStages) & 1))) {
         if (lane == 0) {
           set_error(p.err, kErrTimeout);
           atomicMin(&flags[0], c);
@@ -198,8 +202,8 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
         break;
       }
       const unsigned char* ks = ring + st * C::kStageBytes;
-      const unsigned char* vs = ks + kChunk * C::kRowBytes;
-      const int rows = min(kChunk, ntok - c * kChunk);
+      const unsigned char* vs = ks + C::kChunk * C::kRowBytes;
+      const int rows = min(C::kChunk, ntok - c * C::kChunk);
 
       float sc[C::kRowsPerSlot][GM];
 #pragma unroll
@@ -215,10 +219,11 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
         }
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-          float d = 0.f;
+          float2 d2 = make_float2(0.f, 0.f);  // even and odd elements: two short chains
 #pragma unroll
-          for (int e = 0; e < C::kVec; ++e) d = fmaf(qf[h][e], kf[e], d);
-          d = group_sum<C::kLanesPerRow>(d);
+          for (int e = 0; e < C::kVec; e += 2)
+            d2 = __ffma2_rn(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), d2);
+          float d = group_sum<C::kLanesPerRow>(d2.x + d2.y);
           sc[i][h] = valid ? d : -INFINITY;
         }
       }
@@ -246,7 +251,12 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
             const float w = exp2f(sc[i][h] - m[h]);
             l[h] += w;
 #pragma unroll
-            for (int e = 0; e < C::kVec; ++e) o[h][e] = fmaf(w, vf[e], o[h][e]);
+            for (int e = 0; e < C::kVec; e += 2) {
+              const float2 acc = __ffma2_rn(make_float2(w, w), make_float2(vf[e], vf[e + 1]),
+                                            make_float2(o[h][e], o[h][e + 1]));
+              o[h][e] = acc.x;
+              o[h][e + 1] = acc.y;
+            }
           }
         }
       }
@@ -260,7 +270,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     // A wait ran out: wait (bounded) for the copies still in flight, then leave.
     if (threadIdx.x == kConsumerWarps * 32) {
       for (int c = flags[0]; c < flags[1]; ++c)
-        if (!mbar_wait(&full[c % kStages], (c / kStages) & 1)) break;
+        if (!mbar_wait(&full[c % C::kStages], (c / C::kStages) & 1)) break;
     }
     __syncthreads();
     return;

@@ -138,6 +138,7 @@ CASES = [
     ("bf16", 128, 32, 64, 8, 1500, 512), ("f16", 128, 16, 2, 1, 3000, 0), ("bf16", 64, 32, 16, 2, 1, 0),
     ("bf16", 128, 16, 48, 4, 700, 0), ("f16", 128, 8, 32, 2, 1200, 128), ("bf16", 128, 16, 1, 1, 2500, 256),
     ("f16", 128, 32, 4, 4, 200, 0), ("bf16", 128, 8, 24, 8, 3000, 384),
+    ("f32", 128, 32, 3, 3, 1100, 0), ("f16", 64, 16, 4, 2, 2100, 256), ("bf16", 64, 8, 8, 1, 777, 384),
 ]
 
 
