@@ -51,7 +51,7 @@
  *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16 or 32;
  *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
  *    up to 8 on the CUDA-core decode path and up to 16 on the tensor-core paths
- *    (f16/bf16, head_dim 128).
+ *    (f16/bf16; head_dim 64 or 128 for decode, 128 for prefill).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -86,7 +86,7 @@ typedef struct {
 } pkv_cache_desc;
 
 /* Decode path selection and split-K partition size (NULL config = automatic: tensor
- * cores for f16/bf16 with head_dim 128 and groups <= 16, CUDA cores otherwise). */
+ * cores for f16/bf16 with groups <= 16, CUDA cores otherwise, i.e. for f32). */
 typedef enum { PKV_PATH_AUTO = 0, PKV_PATH_CUDA_CORE = 1, PKV_PATH_TENSOR_CORE = 2 } pkv_path;
 
 typedef struct {

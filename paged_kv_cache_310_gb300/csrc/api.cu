@@ -98,12 +98,12 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
     return fail(PKV_ERR_INVALID_ARG, "decode path %d", path);
   const bool tc_ok = tc_supported(c->dtype, c->head_dim, group, c->block_size);
   // Tensor cores wherever they apply: at G >= 2 QK and PV are real contractions, and at
-  // G = 1 the persistent TMA/tcgen05 kernel still streams K/V slightly faster (0.919 vs
-  // 0.905 of HBM bandwidth on a 64 x 32-head bf16 batch).  f32 and head_dim 64 use CUDA cores.
+  // G = 1 the persistent TMA/tcgen05 kernel still streams K/V slightly faster (0.977 vs
+  // 0.922 of copy bandwidth on a 64 x 32-head bf16 batch).  f32 uses CUDA cores.
   if (path == PKV_PATH_AUTO) path = tc_ok ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
   if (path == PKV_PATH_TENSOR_CORE && !tc_ok)
-    return fail(PKV_ERR_UNSUPPORTED, "tensor-core path needs f16/bf16, head_dim 128, group <= 16 (group %d)",
-                group);
+    return fail(PKV_ERR_UNSUPPORTED,
+                "tensor-core path needs f16/bf16, head_dim 64 or 128, group <= 16 (group %d)", group);
   if (path == PKV_PATH_CUDA_CORE && group > 8)
     return fail(PKV_ERR_UNSUPPORTED, "CUDA-core path supports query-head groups <= 8 (group %d)", group);
   if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * c->block_size > (int64_t{1} << 30))
@@ -430,7 +430,7 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d", num_q_heads,
                 cache->num_kv_heads);
   const int group = num_q_heads / cache->num_kv_heads;
-  if (!tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
+  if (cache->head_dim != 128 || !tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
     return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 128 and query-head groups <= 16");
   if (cache->num_kv_heads > 4095)  // a work-list entry packs the KV head into 12 bits
     return fail(PKV_ERR_UNSUPPORTED, "prefill supports at most 4095 KV heads (%d)", cache->num_kv_heads);

@@ -1,5 +1,5 @@
 // decode_tc.cu -- tensor-core (tcgen05) paged decode attention for f16/bf16 caches,
-// head_dim 128, up to 16 query heads per KV head.
+// head_dim 64 or 128, up to 16 query heads per KV head.
 //
 // What it computes is the same as the CUDA-core path (note-023, Method/Concepts;
 // "Paged Attention" glossary, paragraph 4 and the GQA paragraph): per sequence s, KV
@@ -11,11 +11,14 @@
 // multiply-adds.  At G = 8 streaming K/V at HBM speed needs ~64 TFLOP/s, the whole
 // fp32 CUDA-core rate; as two small dense contractions per 128-token chunk it is a
 // few percent of the tensor cores:
-//   S^T[128 tokens x 16] = K[128 x 128 dims] . Q^T[128 x 16]          (QK, M=128 N=16)
-//   O^T[128 dims x N]    = V^T[128 dims x 128 tokens] . P^T[128 x N]   (PV, M=128)
+//   S^T[128 tokens x 16] = K[128 x D dims] . Q^T[D x 16]          (QK, M=128 N=16)
+//   O^T[D dims x N]      = V^T[D dims x 128 tokens] . P^T[128 x N] (PV, M=128)
 // The query heads of a group are the N dimension of QK (padded to 16).  PV's columns
 // hold each head's probabilities twice, as a rounded part and its remainder (N = 16
-// up to 8 heads, 32 up to 16).
+// up to 8 heads, 32 up to 16).  At D = 64, PV still runs with M = 128: its A operand's
+// second 64-row block is given a leading offset of zero, so it reads the same 64
+// dimensions again and TMEM lanes 64-127 hold a copy that nobody stores (cheaper than
+// the M = 64 accumulator layout, and PV is a small part of the tensor pipe's time).
 //
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
 // head) that work_list_kernel sorts longest first and the CTAs take in snake order;
@@ -24,10 +27,11 @@
 //  * warp 4, producer of Q and K: per 128-token chunk, one lane per physical block
 //    reads the block id (before waiting for a free stage, hiding its latency) and
 //    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
-//    128-byte swizzle) into a 3-stage K ring; blocks past the item's end are loaded
-//    from outside the tensor, which the TMA unit fills with zeros.  It also loads the
+//    128-byte swizzle) into a 96 KB K ring (3 stages at D = 128, 6 at D = 64); blocks
+//    past the item's end are loaded from outside the tensor, which the TMA unit fills
+//    with zeros.  It also loads the
 //    item's 16 query rows.
-//  * warp 6, producer of V: the same for V tiles into a 3-stage V ring.  The rings are
+//  * warp 6, producer of V: the same for V tiles into a V ring of the same size.  The rings are
 //    separate so that a K stage is reused as soon as its chunk's QK completes, long
 //    before the chunk's V is done with: more of the rings stays in flight, and the
 //    kernel is bound by bytes in flight.
@@ -57,41 +61,49 @@ namespace {
 
 constexpr int kThreads = 224;                  // 4 softmax warps, K producer, MMA, V producer
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
-constexpr int kKStages = 3;                    // K ring
-constexpr int kVStages = 3;                    // V ring
 constexpr int kN = 16;                         // MMA N: query heads per group, padded
-// A chunk's K (and V) sits in shared memory as [8-row group][64-column half][8 rows]
-// of 128-byte rows: 16 groups x 2 halves x 1 KB = 32 KB, 128-byte swizzled.  That is
-// the canonical K-major layout for the QK A operand (8-row groups 2 KB apart, halves
-// 1 KB apart) and the MN-major layout for the PV A operand V^T (8-token groups 2 KB
-// apart, 64-dimension blocks 1 KB apart), and one 4-D TMA box fills a whole block.
-constexpr int kGroupBytes = 2048;               // one 8-row group: both halves
-constexpr int kTileBytes = kChunk * 256;        // K or V of one chunk: 32 KB
-constexpr int kQBytes = 2 * kN * 128;          // 4 KB: two halves of 16 rows x 128 B
+constexpr int kQHalfBytes = kN * 128;          // 16 query rows x one 64-dimension block
 // P^T holds each probability as two rounded parts, hi = round(p) and
 // lo = round(p - hi), as separate groups of 8 columns: the PV MMA then sums
 // hi + lo in fp32, so rounding p to 16 bits costs about 2^-17 relative instead of
 // 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (N = 16, the columns are there anyway);
 // up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (N = 32).
 constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
-// K and V have separate rings: a K stage is free once the chunk's QK completed, long
-// before its V (needed until PV completes), so more of the rings stays in flight.
-constexpr int kOffV = kKStages * kTileBytes;
-constexpr int kOffQ = (kKStages + kVStages) * kTileBytes;
-constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 2 * (kKStages + kVStages) + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
-constexpr int kOffRedMax = kOffBar + kNumBars * 8;
-constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
-constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
-constexpr int kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
+// Shared-memory layout for head_dim D (64 or 128).  A chunk's K (and V) sits as
+// [8-row group][64-column block][8 rows] of 128-byte rows, 128-byte swizzled: the
+// canonical K-major layout for the QK A operand (8-row groups kGroupBytes apart,
+// column blocks 1 KB apart) and the MN-major layout for the PV A operand V^T (8-token
+// groups kGroupBytes apart, 64-dimension blocks 1 KB apart), and one 4-D TMA box fills
+// a whole block.  K and V have separate rings: a K stage is free once the chunk's QK
+// completed, long before its V (needed until PV completes), so more of the rings stays
+// in flight; each ring holds 96 KB whatever D is.
+template <int D>
+struct TcLayout {
+  static constexpr int kBlocks = D / 64;                 // 64-column blocks of a row
+  static constexpr int kGroupBytes = 8 * D * 2;          // one 8-row group: all its blocks
+  static constexpr int kTileBytes = kChunk * D * 2;      // K or V of one chunk: 16 or 32 KB
+  static constexpr int kStages = 3 * 128 / D;            // per ring
+  static constexpr int kQBytes = kBlocks * kQHalfBytes;  // the item's query rows
+  static constexpr int kOffV = kStages * kTileBytes;
+  static constexpr int kOffQ = 2 * kStages * kTileBytes;
+  static constexpr int kOffP = kOffQ + 2 * kQBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kNumBars = 4 * kStages + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
+  static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
+  static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
+  static constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
+  static constexpr int kSmemBytes = kOffMisc + 64;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(kOffQ % 1024 == 0 && kSmemBytes <= 227 * 1024, "layout");
+};
+
 struct Bars {
-  uint64_t* kfull;  // [kKStages] K of a chunk landed (TMA tx)
-  uint64_t* kempty; // [kKStages] the chunk's QK done
-  uint64_t* vfull;  // [kVStages] V of a chunk landed
-  uint64_t* vempty; // [kVStages] the chunk's PV done
+  uint64_t* kfull;  // [stages] K of a chunk landed (TMA tx)
+  uint64_t* kempty; // [stages] the chunk's QK done
+  uint64_t* vfull;  // [stages] V of a chunk landed
+  uint64_t* vempty; // [stages] the chunk's PV done
   uint64_t* qfull;  // [2] query tile landed
   uint64_t* qempty; // [2] QK MMAs of that item done
   uint64_t* sfull;  // [2] S ready
@@ -102,14 +114,16 @@ struct Bars {
   uint64_t* drain;  // teardown after an abort
 };
 
+template <int D>
 __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  constexpr int S = TcLayout<D>::kStages;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + TcLayout<D>::kOffBar);
   Bars r;
   r.kfull = b;
-  r.kempty = b + kKStages;
-  r.vfull = b + 2 * kKStages;
-  r.vempty = b + 2 * kKStages + kVStages;
-  r.qfull = b + 2 * (kKStages + kVStages);
+  r.kempty = b + S;
+  r.vfull = b + 2 * S;
+  r.vempty = b + 3 * S;
+  r.qfull = b + 4 * S;
   r.qempty = r.qfull + 2;
   r.sfull = r.qempty + 2;
   r.sfree = r.sfull + 2;
@@ -123,7 +137,7 @@ __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
 struct TcArgs {
   CUtensorMap tk;  // K pool, 4-D view (see make_pool_map): one box = one block's tile
   CUtensorMap tv;  // V pool, same
-  CUtensorMap tq;  // q as [S*Hq rows, 128], box 64 x 16
+  CUtensorMap tq;  // q as [S*Hq rows, head_dim], box 64 x 16
   DecodeParams p;
 };
 
@@ -145,18 +159,22 @@ __device__ __forceinline__ Item unpack_item(int4 e, int part_tokens) {
   return it;
 }
 
-template <typename T, int GM>
+template <typename T, int D, int GM>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
+  using L = TcLayout<D>;
+  constexpr int kKStages = L::kStages, kVStages = L::kStages;
+  constexpr int kGroupBytes = L::kGroupBytes, kTileBytes = L::kTileBytes, kQBytes = L::kQBytes;
+  constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
   extern __shared__ __align__(1024) unsigned char smem[];
   const DecodeParams& p = a.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Bars bars = carve_bars(smem);
-  float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);  // [2][4 warps][kN]
-  float* red_l = reinterpret_cast<float*>(smem + kOffRedL);      // [4 warps][kN]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* kissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);   // K chunks issued
-  int* vissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 12);  // V chunks issued
+  const Bars bars = carve_bars<D>(smem);
+  float* red_max = reinterpret_cast<float*>(smem + L::kOffRedMax);  // [2][4 warps][kN]
+  float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [4 warps][kN]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  int* kissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 8);   // K chunks issued
+  int* vissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 12);  // V chunks issued
   const int G = p.group;
 
   if (threadIdx.x == 0) {
@@ -217,8 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
           unsigned char* qdst = smem + kOffQ + qb * kQBytes;
           const int qrow = it.s * p.num_q_heads + it.g * G;
-          tma_load_2d(qdst, &a.tq, 0, qrow, &bars.qfull[qb], pol_keep);
-          tma_load_2d(qdst + kQBytes / 2, &a.tq, 64, qrow, &bars.qfull[qb], pol_keep);
+#pragma unroll
+          for (int cb = 0; cb < L::kBlocks; ++cb)
+            tma_load_2d(qdst + cb * kQHalfBytes, &a.tq, 64 * cb, qrow, &bars.qfull[qb], pol_keep);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             }
             row = (b * p.num_kv_heads + it.g) * bs;
           }
-          tma_load_4d(smem + st * kTileBytes + lane * bs * 256, &a.tk, row / 8, &bars.kfull[st], pol_stream);
+          tma_load_4d(smem + st * kTileBytes + lane * bs * (D * 2), &a.tk, row / 8, &bars.kfull[st], pol_stream);
         }
         if (lane == 0) *kissued_slot = c + 1;
       }
@@ -282,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             if (b < 0 || b >= p.num_blocks) b = 0;  // the K producer flags it
             row = (b * p.num_kv_heads + it.g) * bs;
           }
-          tma_load_4d(smem + kOffV + st * kTileBytes + lane * bs * 256, &a.tv, row / 8, &bars.vfull[st], pol_stream);
+          tma_load_4d(smem + kOffV + st * kTileBytes + lane * bs * (D * 2), &a.tv, row / 8, &bars.vfull[st],
+                      pol_stream);
         }
         if (lane == 0) *vissued_slot = c + 1;
       }
@@ -300,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
     const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroupBytes, kLayoutSwizzle128);
     const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, 1024, kLayoutSwizzle128);
-    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), 1024, kGroupBytes, kLayoutSwizzle128);
+    // V^T's second 64-dimension block: 1 KB on at D = 128, the same block again at 64
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), D == 128 ? 1024 : 0, kGroupBytes, kLayoutSwizzle128);
     const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, kChunk * 16, kLayoutNone);
     // QK cursor: items walked, chunk within the item, chunks in the item
     ItemCursor qcur;
@@ -347,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            const uint32_t qo = ((kk >> 2) * (kQBytes / 2) + (kk & 3) * 32) >> 4;
+            const uint32_t qo = ((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4;
             mma_f16(tmem + sb * 16, dk + ko, dq + qo, idesc_qk, kk > 0);
           }
           mma_commit(&bars.sfull[sb]);
@@ -386,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     __syncwarp();
   } else {
     // ============================ softmax warps ============================
-    const int t = threadIdx.x;  // TMEM lane: token row of S, dimension row of O
+    const int t = threadIdx.x;  // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float m[GM], lp[GM], alpha[GM], alpha_pend[GM], acc[GM], Lcur[GM], Mcur[GM], Lpend[GM], Mpend[GM];
 #pragma unroll
@@ -418,17 +439,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const float v = GM <= 8 ? o[h] + o[8 + h] : o[h] + olo[h];  // hi part + lo part
         acc[h] = pend_first ? v : fmaf(acc[h], alpha_pend[h], v);
       }
-      if (pend_last) {
+      if (pend_last && t < D) {
         const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G;
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           if (h < G) {
             const size_t row = row0 + h;
             if (pend_nparts == 1) {
-              store_out<T>(p.out, row * 128 + t, acc[h] / Lpend[h], p.out_f32);
+              store_out<T>(p.out, row * D + t, acc[h] / Lpend[h], p.out_f32);
             } else {
               const size_t k = row * p.max_parts + pend_part;
-              p.ws_o[k * 128 + t] = acc[h];
+              p.ws_o[k * D + t] = acc[h];
               if (t == 0) {
                 p.ws_ml[2 * k] = Mpend[h];
                 p.ws_ml[2 * k + 1] = Lpend[h];
@@ -514,10 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (v_ok && t >= rows_valid && t < rows_loaded) {
           unsigned char* vrow = smem + kOffV + (c % kVStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(vrow + 1024)[q] = make_uint4(0, 0, 0, 0);
-          }
+          for (int q = 0; q < 8 * L::kBlocks; ++q)  // 128 bytes per 64-column block, 1 KB apart
+            reinterpret_cast<uint4*>(vrow + (q >> 3) * 1024)[q & 7] = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -637,7 +656,7 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
     }
   }
   // empty contexts: the neutral output, one warp per sequence
-  const int row = p.num_q_heads * 128;
+  const int row = p.num_q_heads * p.head_dim;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int s = warp; s < p.num_seqs; s += kListThreads / 32) {
     if (p.context_lens[s] != 0) continue;
@@ -649,12 +668,12 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
   grid_dependency_wait();
 }
 
-// 2-D map over rows of 128 16-bit elements, box 64 x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16) {
+// 2-D map over rows of head_dim 16-bit elements, box 64 x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16, int head_dim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {128, rows};
-  cuuint64_t strides[1] = {256};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -663,32 +682,39 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int GM>
+template <typename T, int D, int GM>
 cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
+  constexpr int smem = TcLayout<D>::kSmemBytes;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, GM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, D, GM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(decode_tc_kernel<T, GM>, grid, kThreads, kSmemBytes, stream, args);
+  return launch_dependent(decode_tc_kernel<T, D, GM>, grid, kThreads, smem, stream, args);
+}
+
+template <typename T, int D>
+cudaError_t launch_tc_g(const TcArgs& args, int grid, cudaStream_t stream) {
+  const int G = args.p.group;
+  if (G <= 1) return launch_tc_t<T, D, 1>(args, grid, stream);
+  if (G <= 2) return launch_tc_t<T, D, 2>(args, grid, stream);
+  if (G <= 4) return launch_tc_t<T, D, 4>(args, grid, stream);
+  if (G <= 8) return launch_tc_t<T, D, 8>(args, grid, stream);
+  return launch_tc_t<T, D, 16>(args, grid, stream);
 }
 
 template <typename T>
-cudaError_t launch_tc_g(const TcArgs& args, int grid, cudaStream_t stream) {
-  const int G = args.p.group;
-  if (G <= 1) return launch_tc_t<T, 1>(args, grid, stream);
-  if (G <= 2) return launch_tc_t<T, 2>(args, grid, stream);
-  if (G <= 4) return launch_tc_t<T, 4>(args, grid, stream);
-  if (G <= 8) return launch_tc_t<T, 8>(args, grid, stream);
-  return launch_tc_t<T, 16>(args, grid, stream);
+cudaError_t launch_tc_d(const TcArgs& args, int grid, cudaStream_t stream) {
+  return args.p.head_dim == 64 ? launch_tc_g<T, 64>(args, grid, stream) : launch_tc_g<T, 128>(args, grid, stream);
 }
 
 }  // namespace
 
 bool tc_supported(int dtype, int head_dim, int group, int block_size) {
-  return (dtype == PKV_F16 || dtype == PKV_BF16) && head_dim == 128 && group >= 1 && group <= kN &&
+  return (dtype == PKV_F16 || dtype == PKV_BF16) && (head_dim == 64 || head_dim == 128) && group >= 1 &&
+         group <= kN &&
          (block_size == 8 || block_size == 16 || block_size == 32);
 }
 
@@ -697,9 +723,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
-      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
-      !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16))
+  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
+      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
+      !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16, p.head_dim))
     return cudaErrorInvalidValue;
   const int items = p.max_parts * p.num_seqs * p.num_kv_heads;  // upper bound on the list
   const int sms = sm_count();
@@ -708,7 +734,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   cudaError_t e = bf16 ? launch_dependent(work_list_kernel<__nv_bfloat16>, 1, kListThreads, 0, stream, p)
                        : launch_dependent(work_list_kernel<__half>, 1, kListThreads, 0, stream, p);
   if (e != cudaSuccess || grid == 0) return e;
-  return bf16 ? launch_tc_g<__nv_bfloat16>(args, grid, stream) : launch_tc_g<__half>(args, grid, stream);
+  return bf16 ? launch_tc_d<__nv_bfloat16>(args, grid, stream) : launch_tc_d<__half>(args, grid, stream);
 }
 
 }  // namespace pkv

@@ -53,7 +53,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t st
 
 // CUDA-core split-K decode (any supported dtype, head_dim 64/128, group <= 8).
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t stream);
-// Tensor-core (tcgen05) decode: f16/bf16, head_dim 128, group <= 16, persistent CTAs
+// Tensor-core (tcgen05) decode: f16/bf16, head_dim 64/128, group <= 16, persistent CTAs
 // fed by a work list that a one-CTA kernel builds first.  Partitions <= 4096 tokens.
 constexpr int kTcMaxPartition = 4096;
 bool tc_supported(int dtype, int head_dim, int group, int block_size);

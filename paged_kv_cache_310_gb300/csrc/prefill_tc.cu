@@ -662,8 +662,8 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t st
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) ||
-      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) ||
+  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, 128) ||
+      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, 128) ||
       !make_query_map(&args.tq, p.q, p.num_q_heads, p.num_query_tokens, bf16))
     return cudaErrorInvalidValue;
   prefill_list_kernel<<<1, kListThreads, 0, stream>>>(p);

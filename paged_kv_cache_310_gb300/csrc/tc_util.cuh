@@ -145,15 +145,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pool of rows of 128 16-bit elements seen as 4-D: (64 columns, 8 rows, 2 halves,
-// 8-row groups) with byte strides (-, 256, 128, 2048).  A box of (64, 8, 2, bs/8)
-// is one block's tile for one KV head, landing as [group][half][row][64 columns].
-bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16) {
+// Pool of rows of head_dim (64 or 128) 16-bit elements seen as 4-D: (64 columns,
+// 8 rows, 64-column blocks, 8-row groups) with byte strides (-, row, 128, 8 rows).  A
+// box of (64, 8, head_dim/64, bs/8) is one block's tile for one KV head, landing as
+// [group][column block][row][64 columns].
+bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16,
+                   int head_dim) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn || rows % 8) return false;
-  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
-  cuuint64_t strides[3] = {256, 128, 2048};
-  cuuint32_t box[4] = {64, 8, 2, block_size / 8};
+  if (!fn || rows % 8 || (head_dim != 64 && head_dim != 128)) return false;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(head_dim) * 2, blocks = head_dim / 64;
+  cuuint64_t dims[4] = {64, 8, blocks, rows / 8};
+  cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
+  cuuint32_t box[4] = {64, 8, static_cast<cuuint32_t>(blocks), block_size / 8};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -27,7 +27,7 @@ PATH_IDS = {pkv.PATH_CUDA_CORE: "cuda_core", pkv.PATH_TENSOR_CORE: "tensor_core"
 def supported(path, dtype, head_dim, group):
     """The library's supported set per path (include/pagedkv.h)."""
     if path == pkv.PATH_TENSOR_CORE:
-        return dtype in (torch.float16, torch.bfloat16) and head_dim == 128 and group <= 16
+        return dtype in (torch.float16, torch.bfloat16) and head_dim in (64, 128) and group <= 16
     return group <= 8
 
 
@@ -139,6 +139,7 @@ CASES = [
     ("bf16", 128, 16, 48, 4, 700, 0), ("f16", 128, 8, 32, 2, 1200, 128), ("bf16", 128, 16, 1, 1, 2500, 256),
     ("f16", 128, 32, 4, 4, 200, 0), ("bf16", 128, 8, 24, 8, 3000, 384),
     ("f32", 128, 32, 3, 3, 1100, 0), ("f16", 64, 16, 4, 2, 2100, 256), ("bf16", 64, 8, 8, 1, 777, 384),
+    ("bf16", 64, 16, 32, 2, 1800, 512), ("f16", 64, 32, 12, 1, 600, 0),
 ]
 
 
@@ -190,6 +191,32 @@ def test_empty_and_single_token_sequences(path):
             b = int(w.block_tables[s, 0])
             for h in range(w.num_q_heads):
                 assert same_bytes(got[s, h], vc[b, h // 4, 0])
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_head_dim_64_empty_single_and_split(path):
+    """head_dim 64: empty contexts give zeros, one token gives V_0 exactly, and long
+    sequences split into partitions that the merge combines."""
+    ctx = [0, 1, 1300, 17, 256, 257, 700, 64, 1025]
+    keys, owned = workloads.private_layout(ctx, 16)
+    w = workloads.build_from_layout(name="head_dim 64 edges", seed=310_470, dtype="f16", num_q_heads=16,
+                                    num_kv_heads=2, head_dim=64, block_size=16, ctx=ctx, block_keys=keys,
+                                    owned_rows=owned, cow=[], num_blocks=sum(map(len, keys)) + 3, canary=True,
+                                    gen=torch.Generator().manual_seed(310_470))
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=path, part=256)
+    check_close(out, ref, w.dtype)
+    low = decode_only(w, g, w.dtype, path=path, part=256)
+    check_rounded(low, out)
+    got = low.cpu()
+    for s_ in range(w.num_seqs):
+        n = int(w.context_lens[s_])
+        if n == 0:
+            assert (got[s_] == 0).all()
+        if n == 1:
+            b = int(w.block_tables[s_, 0])
+            for h in range(w.num_q_heads):
+                assert same_bytes(got[s_, h], vc[b, h // 8, 0])
 
 
 # ------------------------------------------------------------------------------------
