@@ -483,49 +483,76 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         const int rows_valid = min(kChunk, it.ntok - k * kChunk);
         const bool valid = wok && t < rows_valid;
-        // chunk max over the 128 tokens, per head
+        // Lazy rescale: the running max m of a head only has to bound its scores
+        // loosely (probabilities up to 2^kSlack stay exact enough in hi + lo and
+        // in fp32 sums), so it moves only when some score of the chunk exceeds it
+        // by more than kSlack (always on an item's first chunk, m = -inf).  One
+        // barrier vote decides it for the chunk; most chunks then skip the max
+        // reduction and the rescale.
+        constexpr float kSlack = 8.f;
+        bool quiet = true;
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
-          float v = sv[h];
+          quiet = quiet && (h >= G || !(sv[h] > m[h] + kSlack));
+        }
+        // every softmax warp learns whether all four got here normally, and whether
+        // any head needs a new running max
+        const bool keep = named_barrier_and(1, 128, wok && prev_ok && quiet);
+        if (!keep) {
+          // chunk max over the 128 tokens, per head
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-          if (lane == 0) red_max[(sb * 4 + warp) * kN + h] = v;
+          for (int h = 0; h < GM; ++h) {
+            float v = sv[h];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+            if (lane == 0) red_max[(sb * 4 + warp) * kN + h] = v;
+          }
+          if (!named_barrier_and(1, 128, wok && prev_ok)) {
+            ok = false;
+            break;
+          }
         }
-        // every softmax warp learns whether all four got here normally
-        if (!named_barrier_and(1, 128, wok && prev_ok)) {
-          ok = false;
-          break;
-        }
-        float ph[16], pl[16];
+        float pe[16];
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-          const float* r = red_max + sb * 4 * kN + h;
-          const float cm = fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN]));
-          const float mn = fmaxf(m[h], cm);
-          alpha[h] = exp2f(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
+          float mn = m[h];
+          if (!keep) {
+            const float* r = red_max + sb * 4 * kN + h;
+            mn = fmaxf(mn, fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN])));
+          }
+          alpha[h] = keep ? 1.f : exp2_approx(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
           m[h] = mn;
-          const float pe = h < G ? exp2f(sv[h] - mn) : 0.f;
-          ph[h] = round_to<T>(pe);
-          pl[h] = round_to<T>(pe - ph[h]);  // pe - ph[h] is exact in fp32
-          lp[h] = fmaf(lp[h], alpha[h], pe);
+          pe[h] = h < G ? exp2_approx(sv[h] - mn) : 0.f;
+          lp[h] = fmaf(lp[h], alpha[h], pe[h]);
         }
 #pragma unroll
-        for (int h = GM; h < 16; ++h) ph[h] = pl[h] = 0.f;
+        for (int h = GM; h < 16; ++h) pe[h] = 0.f;
+        // hi = round(p) and lo = round(p - hi) (p - hi is exact in fp32), two heads a word
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (2 * i < GM) {
+            float h0, h1;
+            hw[i] = pack2_split<T>(pe[2 * i], pe[2 * i + 1], h0, h1);
+            lw[i] = pack2<T>(pe[2 * i] - h0, pe[2 * i + 1] - h1);
+          } else {
+            hw[i] = lw[i] = 0u;
+          }
+        }
         // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns a group
         unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
-        auto put8 = [&](int group, const float* v) {
-          *reinterpret_cast<uint4*>(pdst + group * kChunk * 16) =
-              make_uint4(pack2<T>(v[0], v[1]), pack2<T>(v[2], v[3]), pack2<T>(v[4], v[5]), pack2<T>(v[6], v[7]));
+        auto put8 = [&](int group, const uint32_t* w) {
+          *reinterpret_cast<uint4*>(pdst + group * kChunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
         };
         if (GM <= 8) {
-          put8(0, ph);
-          put8(1, pl);
+          put8(0, hw);
+          put8(1, lw);
         } else {
-          put8(0, ph);
-          put8(1, ph + 8);
-          put8(2, pl);
-          put8(3, pl + 8);
+          put8(0, hw);
+          put8(1, hw + 4);
+          put8(2, lw);
+          put8(3, lw + 4);
         }
         // rows of the last loaded block past the context end: zero their V rows
         const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
