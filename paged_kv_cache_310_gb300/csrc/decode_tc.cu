@@ -92,8 +92,9 @@ struct TcLayout {
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
   static constexpr int kNumBars = 4 * kStages + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
   static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
-  static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
-  static constexpr int kOffMisc = kOffRedL + 4 * kN * 4;
+  static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;  // [2 chunk slots][4 warps][kN]
+  static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;    // [2 chunk slots][kN]
+  static constexpr int kOffMisc = kOffMTot + 2 * kN * 4;
   static constexpr int kSmemBytes = kOffMisc + 64;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(kOffQ % 1024 == 0 && kSmemBytes <= 227 * 1024, "layout");
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Bars bars = carve_bars<D>(smem);
   float* red_max = reinterpret_cast<float*>(smem + L::kOffRedMax);  // [2][4 warps][kN]
-  float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [4 warps][kN]
+  float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [2 chunk slots][4 warps][kN]
+  float* red_mtot = reinterpret_cast<float*>(smem + L::kOffMTot);   // [2 chunk slots][kN]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int* kissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 8);   // K chunks issued
@@ -409,15 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // ============================ softmax warps ============================
     const int t = threadIdx.x;  // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m[GM], lp[GM], alpha[GM], alpha_pend[GM], acc[GM], Lcur[GM], Mcur[GM], Lpend[GM], Mpend[GM];
+    float m[GM], lp[GM], alpha[GM], alpha_pend[GM], acc[GM];
 #pragma unroll
     for (int h = 0; h < GM; ++h) {
       m[h] = -INFINITY; lp[h] = 0.f; alpha[h] = 0.f; alpha_pend[h] = 0.f; acc[h] = 0.f;
-      Lcur[h] = 1.f; Mcur[h] = 0.f; Lpend[h] = 1.f; Mpend[h] = 0.f;
     }
     // pending chunk (its O not yet consumed): item fields and flags
     int pend_s = 0, pend_g = 0, pend_part = 0, pend_nparts = 0;
-    bool pend_first = false, pend_last = false;
+    bool pend_first = false, pend_last = false, pend_keep = false;
     int c = 0;
     bool ok = true;
 
@@ -437,22 +438,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
         const float v = GM <= 8 ? o[h] + o[8 + h] : o[h] + olo[h];  // hi part + lo part
-        acc[h] = pend_first ? v : fmaf(acc[h], alpha_pend[h], v);
+        acc[h] = pend_first ? v : pend_keep ? acc[h] + v : fmaf(acc[h], alpha_pend[h], v);
       }
       if (pend_last && t < D) {
+        // the item's totals, left in slot cp & 1 at its last chunk
+        const float* rl = red_l + (cp & 1) * 4 * kN;
         const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G;
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           if (h < G) {
+            const float l = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
             const size_t row = row0 + h;
             if (pend_nparts == 1) {
-              store_out<T>(p.out, row * D + t, acc[h] / Lpend[h], p.out_f32);
+              store_out<T>(p.out, row * D + t, acc[h] / l, p.out_f32);
             } else {
               const size_t k = row * p.max_parts + pend_part;
               p.ws_o[k * D + t] = acc[h];
               if (t == 0) {
-                p.ws_ml[2 * k] = Mpend[h];
-                p.ws_ml[2 * k + 1] = Lpend[h];
+                p.ws_ml[2 * k] = red_mtot[(cp & 1) * kN + h];
+                p.ws_ml[2 * k + 1] = l;
               }
             }
           }
@@ -465,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     ItemCursor cur;
     for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
       const Item it = unpack_item(cur.cur, p.part_tokens);
+      // padded heads (h >= G) get m = +inf: their scores then come out as -inf and
+      // their probabilities as 0 without a test (their l and O are never stored)
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
-        m[h] = -INFINITY;
+        m[h] = h < G ? -INFINITY : INFINITY;
         lp[h] = 0.f;
       }
       for (int k = 0; k < it.nchunks; ++k, ++c) {
@@ -490,19 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // barrier vote decides it for the chunk; most chunks then skip the max
         // reduction and the rescale.
         constexpr float kSlack = 8.f;
-        bool quiet = true;
+        float x[GM], pe[16];  // x = score - running max (log2 domain), -inf past the context end
+        float excess = -INFINITY;
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-          sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
-          quiet = quiet && (h >= G || !(sv[h] > m[h] + kSlack));
+          x[h] = valid ? fmaf(sv[h], p.scale_log2, -m[h]) : -INFINITY;
+          excess = fmaxf(excess, x[h]);
         }
         // every softmax warp learns whether all four got here normally, and whether
         // any head needs a new running max
-        const bool keep = named_barrier_and(1, 128, wok && prev_ok && quiet);
-        if (!keep) {
+        const bool keep = named_barrier_and(1, 128, wok && prev_ok && !(excess > kSlack));
+        if (keep) {
+#pragma unroll
+          for (int h = 0; h < GM; ++h) {
+            pe[h] = exp2_approx(x[h]);
+            lp[h] += pe[h];
+          }
+        } else {
           // chunk max over the 128 tokens, per head
 #pragma unroll
           for (int h = 0; h < GM; ++h) {
+            sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
             float v = sv[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -512,19 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             ok = false;
             break;
           }
-        }
-        float pe[16];
 #pragma unroll
-        for (int h = 0; h < GM; ++h) {
-          float mn = m[h];
-          if (!keep) {
+          for (int h = 0; h < GM; ++h) {
             const float* r = red_max + sb * 4 * kN + h;
-            mn = fmaxf(mn, fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN])));
+            const float mn = fmaxf(m[h], fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN])));
+            alpha[h] = exp2_approx(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
+            m[h] = mn;
+            pe[h] = exp2_approx(sv[h] - mn);
+            lp[h] = fmaf(lp[h], alpha[h], pe[h]);
           }
-          alpha[h] = keep ? 1.f : exp2_approx(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
-          m[h] = mn;
-          pe[h] = h < G ? exp2_approx(sv[h] - mn) : 0.f;
-          lp[h] = fmaf(lp[h], alpha[h], pe[h]);
         }
 #pragma unroll
         for (int h = GM; h < 16; ++h) pe[h] = 0.f;
@@ -554,47 +564,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           put8(2, lw);
           put8(3, lw + 4);
         }
-        // rows of the last loaded block past the context end: zero their V rows
-        const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
-        // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
-        const bool v_ok = rows_valid >= rows_loaded ||
-                          __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kVStages], (c / kVStages) & 1, abort_flag, p.err));
-        if (v_ok && t >= rows_valid && t < rows_loaded) {
-          unsigned char* vrow = smem + kOffV + (c % kVStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
+        // rows of the last loaded block past the context end: zero their V rows (only an
+        // item's last chunk can have them)
+        const bool last = k == it.nchunks - 1;
+        if (last && rows_valid < kChunk) {
+          const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
+          // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
+          const bool v_ok = rows_valid >= rows_loaded ||
+                            __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kVStages], (c / kVStages) & 1,
+                                                              abort_flag, p.err));
+          if (v_ok && t >= rows_valid && t < rows_loaded) {
+            unsigned char* vrow = smem + kOffV + (c % kVStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
 #pragma unroll
-          for (int q = 0; q < 8 * L::kBlocks; ++q)  // 128 bytes per 64-column block, 1 KB apart
-            reinterpret_cast<uint4*>(vrow + (q >> 3) * 1024)[q & 7] = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < 8 * L::kBlocks; ++q)  // 128 bytes per 64-column block, 1 KB apart
+              reinterpret_cast<uint4*>(vrow + (q >> 3) * 1024)[q & 7] = make_uint4(0, 0, 0, 0);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.pfull[sb]);
 
-        const bool last = k == it.nchunks - 1;
-        if (last) {  // totals of this item (row sums over the 128 lanes)
+        if (last) {  // this item's totals (row sums per warp, running max) into slot c & 1
 #pragma unroll
           for (int h = 0; h < GM; ++h) {
             float v = lp[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red_l[warp * kN + h] = v;
+            if (lane == 0) red_l[((c & 1) * 4 + warp) * kN + h] = v;
+            if (t == 0) red_mtot[(c & 1) * kN + h] = m[h];
           }
           named_barrier_sync(1, 128);
-#pragma unroll
-          for (int h = 0; h < GM; ++h) {
-            Lcur[h] = (red_l[h] + red_l[kN + h]) + (red_l[2 * kN + h] + red_l[3 * kN + h]);
-            Mcur[h] = m[h];
-          }
         }
         if (c >= 1) prev_ok = consume(c - 1);
         // chunk c becomes the pending one
+        if (!keep) {
 #pragma unroll
-        for (int h = 0; h < GM; ++h) {
-          alpha_pend[h] = alpha[h];
-          if (last) {
-            Lpend[h] = Lcur[h];
-            Mpend[h] = Mcur[h];
-          }
+          for (int h = 0; h < GM; ++h) alpha_pend[h] = alpha[h];
         }
+        pend_keep = keep;
         pend_first = k == 0;
         pend_last = last;
         pend_s = it.s;
