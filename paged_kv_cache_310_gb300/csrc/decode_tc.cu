@@ -40,11 +40,12 @@
 //    memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed; commits
 //    release the ring stages and signal the softmax warps.
 //  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
-//    chunk max across the 128 tokens (shuffles + shared memory), online-softmax
-//    rescale, probabilities split into two parts rounded to the cache dtype
-//    (hi = round(p), lo = round(p - hi)) into P^T (shared memory), then read O row t
-//    (dimension t) of the previous chunk, add its hi and lo columns and accumulate in
-//    registers with the rescale factor.
+//    vote on whether any score exceeds its head's running max by more than 2^8 (if
+//    so, chunk max across the 128 tokens by shuffles + shared memory and an
+//    online-softmax rescale), probabilities split into two parts rounded to the cache
+//    dtype (hi = round(p), lo = round(p - hi)) into P^T (shared memory), then read O
+//    row t (dimension t) of the previous chunk, add its hi and lo columns and
+//    accumulate in registers with the rescale factor.
 //  Rows of the last block past the context end hold real cache data; the softmax
 //  warps zero those V rows in shared memory before PV (a NaN there would survive a
 //  zero weight).

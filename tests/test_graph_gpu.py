@@ -25,10 +25,11 @@ def capture(fn):
     return graph
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
 @pytest.mark.parametrize("path", [pkv.PATH_CUDA_CORE, pkv.PATH_TENSOR_CORE], ids=["cuda_core", "tensor_core"])
-def test_decode_step_replays_in_a_graph(path):
+def test_decode_step_replays_in_a_graph(path, head_dim):
     w = workloads.random_workload(310_470, num_seqs=9, max_len=1500, min_len=1, num_q_heads=16, num_kv_heads=4,
-                                  head_dim=128, block_size=16, dtype="bf16", canary=False)
+                                  head_dim=head_dim, block_size=16, dtype="bf16", canary=False)
     g = w.to("cuda")
     out = torch.empty(g.q.shape, dtype=torch.float32, device="cuda")
 

@@ -2,7 +2,7 @@
 deterministic, and a race in their pipelines (a stage reused too early, a buffer read
 before it landed) would show up as a differing repeat.  Decode runs on the GQA-70B-like
 batch (tensor cores, dependent launches after the append) and with split-K partitions
-on both paths; prefill on a chunked-prefill batch."""
+on both paths at both head sizes; prefill on a chunked-prefill batch."""
 import pytest
 import torch
 
@@ -36,10 +36,11 @@ def test_decode_steps_repeat_bit_identically():
     repeat_equal(step, out, 60)
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
 @pytest.mark.parametrize("path", [pkv.PATH_CUDA_CORE, pkv.PATH_TENSOR_CORE], ids=["cuda_core", "tensor_core"])
-def test_split_decode_repeats_bit_identically(path):
+def test_split_decode_repeats_bit_identically(path, head_dim):
     w = workloads.random_workload(310_480, num_seqs=24, max_len=3000, min_len=1, num_q_heads=32, num_kv_heads=8,
-                                  head_dim=128, block_size=16, dtype="bf16", canary=False)
+                                  head_dim=head_dim, block_size=16, dtype="bf16", canary=False)
     g = w.to("cuda")
     out = torch.empty(g.q.shape, dtype=torch.float32, device="cuda")
 
