@@ -60,7 +60,6 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 224;                  // 4 softmax warps, K producer, MMA, V producer
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
 constexpr int kN = 16;                         // MMA N: query heads per group, padded
 constexpr int kQHalfBytes = kN * 128;          // 16 query rows x one 64-dimension block
@@ -71,6 +70,18 @@ constexpr int kQHalfBytes = kN * 128;          // 16 query rows x one 64-dimensi
 // up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (N = 32).
 constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
+
+// Roles: warps 0-3 softmax, 4 producer of Q and K, 5 MMA, 6 producer of V, and from
+// 8 query heads per KV head warps 7-10 softmax too: a warp reads the TMEM lane
+// quarter of its index mod 4, so two warps share each quarter (each 32 tokens) and
+// take half of the heads each, which halves the softmax work per thread.
+template <int GM>
+struct TcRoles {
+  static constexpr int kSplit = GM >= 8 ? 2 : 1;      // softmax warps per lane quarter
+  static constexpr int kHeads = GM / kSplit;          // query heads per softmax thread
+  static constexpr int kSoftmaxThreads = 128 * kSplit;
+  static constexpr int kThreads = kSoftmaxThreads + 96;
+};
 
 // Shared-memory layout for head_dim D (64 or 128).  A chunk's K (and V) sits as
 // [8-row group][64-column block][8 rows] of 128-byte rows, 128-byte swizzled: the
@@ -162,8 +173,9 @@ __device__ __forceinline__ Item unpack_item(int4 e, int part_tokens) {
 }
 
 template <typename T, int D, int GM>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
   using L = TcLayout<D>;
+  using R = TcRoles<GM>;
   constexpr int kKStages = L::kStages, kVStages = L::kStages;
   constexpr int kGroupBytes = L::kGroupBytes, kTileBytes = L::kTileBytes, kQBytes = L::kQBytes;
   constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
@@ -193,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_init(&bars.qfull[i], 1);
       mbar_init(&bars.qempty[i], 1);
       mbar_init(&bars.sfull[i], 1);
-      mbar_init(&bars.sfree[i], 4);
-      mbar_init(&bars.pfull[i], 4);
+      mbar_init(&bars.sfree[i], 4 * R::kSplit);
+      mbar_init(&bars.pfull[i], 4 * R::kSplit);
       mbar_init(&bars.ofull[i], 1);
-      mbar_init(&bars.ofree[i], 4);
+      mbar_init(&bars.ofree[i], 4 * R::kSplit);
     }
     *abort_flag = 0;
     *kissued_slot = 0;
@@ -410,11 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     __syncwarp();
   } else {
     // ============================ softmax warps ============================
-    const int t = threadIdx.x;  // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float m[GM], lp[GM], alpha[GM], alpha_pend[GM], acc[GM];
+    constexpr int HG = R::kHeads;              // heads of this thread: h0 .. h0 + HG - 1
+    constexpr int NS = R::kSoftmaxThreads;     // threads in the softmax barriers
+    const int quarter = warp & 3;              // TMEM lane quarter this warp may read
+    const int h0 = warp >= 7 ? HG : 0;         // first head (the second warp of a quarter: the upper half)
+    const int t = quarter * 32 + lane;         // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float m[HG], lp[HG], alpha[HG], alpha_pend[HG], acc[HG];
 #pragma unroll
-    for (int h = 0; h < GM; ++h) {
+    for (int h = 0; h < HG; ++h) {
       m[h] = -INFINITY; lp[h] = 0.f; alpha[h] = 0.f; alpha_pend[h] = 0.f; acc[h] = 0.f;
     }
     // pending chunk (its O not yet consumed): item fields and flags
@@ -430,24 +446,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err)))
         return false;
       tc_fence_after();
-      float o[16], olo[16];
-      tmem_load16(lane_base + 32 + pb * 32, o);
-      if (GM > 8) tmem_load16(lane_base + 32 + pb * 32 + 16, olo);
+      // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16
+      const uint32_t ob = lane_base + 32 + pb * 32 + h0;
+      float o[HG], olo[HG];
+      if (GM <= 8) {
+        float a4[4], b4[4];
+        tmem_load4x2(ob, ob + 8, a4, b4);
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          o[h] = a4[h];
+          olo[h] = b4[h];
+        }
+      } else {
+        tmem_load8x2(ob, ob + 16, o, olo);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ofree[pb]);
 #pragma unroll
-      for (int h = 0; h < GM; ++h) {
-        const float v = GM <= 8 ? o[h] + o[8 + h] : o[h] + olo[h];  // hi part + lo part
+      for (int h = 0; h < HG; ++h) {
+        const float v = o[h] + olo[h];  // hi part + lo part
         acc[h] = pend_first ? v : pend_keep ? acc[h] + v : fmaf(acc[h], alpha_pend[h], v);
       }
       if (pend_last && t < D) {
         // the item's totals, left in slot cp & 1 at its last chunk
-        const float* rl = red_l + (cp & 1) * 4 * kN;
-        const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G;
+        const float* rl = red_l + (cp & 1) * 4 * kN + h0;
+        const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G + h0;
 #pragma unroll
-        for (int h = 0; h < GM; ++h) {
-          if (h < G) {
+        for (int h = 0; h < HG; ++h) {
+          if (h0 + h < G) {
             const float l = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
             const size_t row = row0 + h;
             if (pend_nparts == 1) {
@@ -456,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               const size_t k = row * p.max_parts + pend_part;
               p.ws_o[k * D + t] = acc[h];
               if (t == 0) {
-                p.ws_ml[2 * k] = red_mtot[(cp & 1) * kN + h];
+                p.ws_ml[2 * k] = red_mtot[(cp & 1) * kN + h0 + h];
                 p.ws_ml[2 * k + 1] = l;
               }
             }
@@ -473,17 +500,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       // padded heads (h >= G) get m = +inf: their scores then come out as -inf and
       // their probabilities as 0 without a test (their l and O are never stored)
 #pragma unroll
-      for (int h = 0; h < GM; ++h) {
-        m[h] = h < G ? -INFINITY : INFINITY;
+      for (int h = 0; h < HG; ++h) {
+        m[h] = h0 + h < G ? -INFINITY : INFINITY;
         lp[h] = 0.f;
       }
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
         const bool wok = __all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err));
-        float sv[16];
+        float sv[HG];
         if (wok) {
           tc_fence_after();
-          tmem_load16(lane_base + sb * 16, sv);
+          if (HG <= 4) {
+            float s4[4];
+            tmem_load4(lane_base + sb * 16 + h0, s4);
+#pragma unroll
+            for (int h = 0; h < HG; ++h) sv[h] = s4[h];
+          } else {
+            tmem_load8(lane_base + sb * 16 + h0, sv);
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.sfree[sb]);
@@ -497,39 +531,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         // barrier vote decides it for the chunk; most chunks then skip the max
         // reduction and the rescale.
         constexpr float kSlack = 8.f;
-        float x[GM], pe[16];  // x = score - running max (log2 domain), -inf past the context end
+        float x[HG], pe[HG];  // x = score - running max (log2 domain), -inf past the context end
         float excess = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < GM; ++h) {
+        for (int h = 0; h < HG; ++h) {
           x[h] = valid ? fmaf(sv[h], p.scale_log2, -m[h]) : -INFINITY;
           excess = fmaxf(excess, x[h]);
         }
-        // every softmax warp learns whether all four got here normally, and whether
-        // any head needs a new running max
-        const bool keep = named_barrier_and(1, 128, wok && prev_ok && !(excess > kSlack));
+        // every softmax warp learns whether all got here normally, and whether any
+        // head needs a new running max
+        const bool keep = named_barrier_and(1, NS, wok && prev_ok && !(excess > kSlack));
         if (keep) {
 #pragma unroll
-          for (int h = 0; h < GM; ++h) {
+          for (int h = 0; h < HG; ++h) {
             pe[h] = exp2_approx(x[h]);
             lp[h] += pe[h];
           }
         } else {
           // chunk max over the 128 tokens, per head
 #pragma unroll
-          for (int h = 0; h < GM; ++h) {
+          for (int h = 0; h < HG; ++h) {
             sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
             float v = sv[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-            if (lane == 0) red_max[(sb * 4 + warp) * kN + h] = v;
+            if (lane == 0) red_max[(sb * 4 + quarter) * kN + h0 + h] = v;
           }
-          if (!named_barrier_and(1, 128, wok && prev_ok)) {
+          if (!named_barrier_and(1, NS, wok && prev_ok)) {
             ok = false;
             break;
           }
 #pragma unroll
-          for (int h = 0; h < GM; ++h) {
-            const float* r = red_max + sb * 4 * kN + h;
+          for (int h = 0; h < HG; ++h) {
+            const float* r = red_max + sb * 4 * kN + h0 + h;
             const float mn = fmaxf(m[h], fmaxf(fmaxf(r[0], r[kN]), fmaxf(r[2 * kN], r[3 * kN])));
             alpha[h] = exp2_approx(m[h] - mn);  // 0 on the item's first chunk (m = -inf)
             m[h] = mn;
@@ -537,38 +571,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             lp[h] = fmaf(lp[h], alpha[h], pe[h]);
           }
         }
+        // hi = round(p) and lo = round(p - hi) (p - hi is exact in fp32), two heads a
+        // word; words past this thread's heads are zero
+        uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int h = GM; h < 16; ++h) pe[h] = 0.f;
-        // hi = round(p) and lo = round(p - hi) (p - hi is exact in fp32), two heads a word
-        uint32_t hw[8], lw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (2 * i < GM) {
-            float h0, h1;
-            hw[i] = pack2_split<T>(pe[2 * i], pe[2 * i + 1], h0, h1);
-            lw[i] = pack2<T>(pe[2 * i] - h0, pe[2 * i + 1] - h1);
+        for (int i = 0; i < 4; ++i) {
+          if (2 * i < HG) {
+            const float a = pe[2 * i], b = 2 * i + 1 < HG ? pe[2 * i + 1] : 0.f;
+            float ha, hb;
+            hw[i] = pack2_split<T>(a, b, ha, hb);
+            lw[i] = pack2<T>(a - ha, b - hb);
           } else {
             hw[i] = lw[i] = 0u;
           }
         }
-        // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns a group
+        // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns (16
+        // bytes) a group: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-7][hi 8-15][lo 0-7][lo
+        // 8-15] for 16
         unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
-        auto put8 = [&](int group, const uint32_t* w) {
-          *reinterpret_cast<uint4*>(pdst + group * kChunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-        };
-        if (GM <= 8) {
-          put8(0, hw);
-          put8(1, lw);
+        if (GM <= 4) {
+          *reinterpret_cast<uint4*>(pdst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(pdst + kChunk * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        } else if (GM == 8) {  // each of the two warps writes its four heads' half of a group
+          *reinterpret_cast<uint2*>(pdst + h0 * 2) = make_uint2(hw[0], hw[1]);
+          *reinterpret_cast<uint2*>(pdst + kChunk * 16 + h0 * 2) = make_uint2(lw[0], lw[1]);
         } else {
-          put8(0, hw);
-          put8(1, hw + 4);
-          put8(2, lw);
-          put8(3, lw + 4);
+          const int gh = h0 / 8;  // this warp's column group of hi parts
+          *reinterpret_cast<uint4*>(pdst + gh * kChunk * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(pdst + (2 + gh) * kChunk * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         // rows of the last loaded block past the context end: zero their V rows (only an
-        // item's last chunk can have them)
+        // item's last chunk can have them; the first warp of each quarter does it)
         const bool last = k == it.nchunks - 1;
-        if (last && rows_valid < kChunk) {
+        if (last && rows_valid < kChunk && h0 == 0) {
           const int rows_loaded = min(kChunk, (rows_valid + p.block_size - 1) / p.block_size * p.block_size);
           // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
           const bool v_ok = rows_valid >= rows_loaded ||
@@ -585,22 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.pfull[sb]);
 
-        if (last) {  // this item's totals (row sums per warp, running max) into slot c & 1
+        if (last) {  // this item's totals (row sums per lane quarter, running max) into slot c & 1
 #pragma unroll
-          for (int h = 0; h < GM; ++h) {
+          for (int h = 0; h < HG; ++h) {
             float v = lp[h];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red_l[((c & 1) * 4 + warp) * kN + h] = v;
-            if (t == 0) red_mtot[(c & 1) * kN + h] = m[h];
+            if (lane == 0) red_l[((c & 1) * 4 + quarter) * kN + h0 + h] = v;
+            if (t == 0) red_mtot[(c & 1) * kN + h0 + h] = m[h];
           }
-          named_barrier_sync(1, 128);
+          named_barrier_sync(1, NS);
         }
         if (c >= 1) prev_ok = consume(c - 1);
         // chunk c becomes the pending one
         if (!keep) {
 #pragma unroll
-          for (int h = 0; h < GM; ++h) alpha_pend[h] = alpha[h];
+          for (int h = 0; h < HG; ++h) alpha_pend[h] = alpha[h];
         }
         pend_keep = keep;
         pend_first = k == 0;
@@ -727,7 +762,7 @@ cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(decode_tc_kernel<T, D, GM>, grid, kThreads, smem, stream, args);
+  return launch_dependent(decode_tc_kernel<T, D, GM>, grid, TcRoles<GM>::kThreads, smem, stream, args);
 }
 
 template <typename T, int D>
