@@ -72,12 +72,12 @@ constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 c
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
 // Roles: warps 0-3 softmax, 4 producer of Q and K, 5 MMA, 6 producer of V, and from
-// 8 query heads per KV head warps 7-10 softmax too: a warp reads the TMEM lane
+// 4 query heads per KV head warps 7-10 softmax too: a warp reads the TMEM lane
 // quarter of its index mod 4, so two warps share each quarter (each 32 tokens) and
 // take half of the heads each, which halves the softmax work per thread.
 template <int GM>
 struct TcRoles {
-  static constexpr int kSplit = GM >= 8 ? 2 : 1;      // softmax warps per lane quarter
+  static constexpr int kSplit = GM >= 4 ? 2 : 1;      // softmax warps per lane quarter
   static constexpr int kHeads = GM / kSplit;          // query heads per softmax thread
   static constexpr int kSoftmaxThreads = 128 * kSplit;
   static constexpr int kThreads = kSoftmaxThreads + 96;
@@ -216,6 +216,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+  // P's columns of heads a thread never writes (past the group, when two warps share
+  // a group of 8 columns) must read as zero
+  for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += R::kThreads)
+    reinterpret_cast<uint4*>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -449,13 +454,13 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16
       const uint32_t ob = lane_base + 32 + pb * 32 + h0;
       float o[HG], olo[HG];
-      if (GM <= 8) {
+      if (GM <= 8) {  // 4-column aligned loads; a pair at column 2 is picked from them
         float a4[4], b4[4];
-        tmem_load4x2(ob, ob + 8, a4, b4);
+        tmem_load4x2(ob - (h0 & 3), ob - (h0 & 3) + 8, a4, b4);
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-          o[h] = a4[h];
-          olo[h] = b4[h];
+          o[h] = (h0 & 2) ? a4[(2 + h) & 3] : a4[h];
+          olo[h] = (h0 & 2) ? b4[(2 + h) & 3] : b4[h];
         }
       } else {
         tmem_load8x2(ob, ob + 16, o, olo);
@@ -510,11 +515,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         float sv[HG];
         if (wok) {
           tc_fence_after();
-          if (HG <= 4) {
+          if (HG <= 4) {  // 4-column aligned load; a pair at column 2 is picked from it
             float s4[4];
-            tmem_load4(lane_base + sb * 16 + h0, s4);
+            tmem_load4(lane_base + sb * 16 + (h0 & ~3), s4);
 #pragma unroll
-            for (int h = 0; h < HG; ++h) sv[h] = s4[h];
+            for (int h = 0; h < HG; ++h) sv[h] = (h0 & 2) ? s4[(2 + h) & 3] : s4[h];
           } else {
             tmem_load8(lane_base + sb * 16 + h0, sv);
           }
@@ -589,9 +594,12 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         // bytes) a group: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-7][hi 8-15][lo 0-7][lo
         // 8-15] for 16
         unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
-        if (GM <= 4) {
+        if (R::kSplit == 1) {
           *reinterpret_cast<uint4*>(pdst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(pdst + kChunk * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        } else if (GM == 4) {  // each of the two warps writes its two heads of a group
+          *reinterpret_cast<uint32_t*>(pdst + h0 * 2) = hw[0];
+          *reinterpret_cast<uint32_t*>(pdst + kChunk * 16 + h0 * 2) = lw[0];
         } else if (GM == 8) {  // each of the two warps writes its four heads' half of a group
           *reinterpret_cast<uint2*>(pdst + h0 * 2) = make_uint2(hw[0], hw[1]);
           *reinterpret_cast<uint2*>(pdst + kChunk * 16 + h0 * 2) = make_uint2(lw[0], lw[1]);
