@@ -557,9 +557,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
 #pragma unroll
           for (int h = 0; h < HG; ++h) {
             sv[h] = valid ? sv[h] * p.scale_log2 : -INFINITY;
-            float v = sv[h];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+            const float v = warp_max(sv[h]);
             if (lane == 0) red_max[(sb * 4 + quarter) * kN + h0 + h] = v;
           }
           if (!named_barrier_and(1, NS, wok && prev_ok)) {

@@ -94,6 +94,14 @@ __device__ __forceinline__ uint32_t pack2_split<__half>(float a, float b, float&
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Maximum over the warp's 32 lanes in one instruction (sm_100 family); like fmaxf,
+// NaN inputs are ignored.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; exp2(-inf) = 0).
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
