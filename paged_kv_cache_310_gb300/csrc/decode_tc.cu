@@ -627,13 +627,12 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (lane == 0) mbar_arrive(&bars.pfull[sb]);
 
         if (last) {  // this item's totals (row sums per lane quarter, running max) into slot c & 1
+          const float lsum = warp_sum_scatter<HG>(lp, lane);  // head warp_sum_index<HG>(lane)
+          if ((lane & (32 / HG - 1)) == 0)
+            red_l[((c & 1) * 4 + quarter) * kN + h0 + warp_sum_index<HG>(lane)] = lsum;
+          if (t == 0) {
 #pragma unroll
-          for (int h = 0; h < HG; ++h) {
-            float v = lp[h];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0) red_l[((c & 1) * 4 + quarter) * kN + h0 + h] = v;
-            if (t == 0) red_mtot[(c & 1) * kN + h0 + h] = m[h];
+            for (int h = 0; h < HG; ++h) red_mtot[(c & 1) * kN + h0 + h] = m[h];
           }
           named_barrier_sync(1, NS);
         }

@@ -102,6 +102,42 @@ __device__ __forceinline__ float warp_max(float v) {
   return r;
 }
 
+// Sums each of a lane's N values (N a power of two <= 32) over the warp's 32 lanes
+// by a reduce-scatter: at each step a lane keeps half of its values and adds its
+// partner's copy of that half, then a butterfly over the remaining lane bits.  Returns
+// in every lane the total of value warp_sum_index<N>(lane), after N - 1 + 5 - log2 N
+// shuffles instead of 5 N.
+template <int N>
+__device__ __forceinline__ float warp_sum_scatter(const float* v, int lane) {
+  float a[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) a[i] = v[i];
+  int off = 16;
+#pragma unroll
+  for (int n = N; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = lane & off;  // this lane keeps the upper half
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? a[i] : a[i + n / 2];
+      const float keep = upper ? a[i + n / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = a[0];
+#pragma unroll
+  for (; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
+}
+
+// Which of the N values warp_sum_scatter<N> leaves in `lane`.
+template <int N>
+__device__ __forceinline__ int warp_sum_index(int lane) {
+  int h = 0;
+#pragma unroll
+  for (int n = N, off = 16; n > 1; n >>= 1, off >>= 1) h = 2 * h + ((lane & off) ? 1 : 0);
+  return h;
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; exp2(-inf) = 0).
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
