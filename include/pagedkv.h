@@ -51,7 +51,7 @@
  *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16 or 32;
  *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
  *    up to 8 on the CUDA-core decode path and up to 16 on the tensor-core paths
- *    (f16/bf16; head_dim 64 or 128 for decode, 128 for prefill).
+ *    (f16/bf16, head_dim 64 or 128).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -249,7 +249,7 @@ size_t paged_attention_no_alloc_limit(void);
  * query_start: device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0 and
  * query_start[num_seqs] = num_query_tokens.  A sequence with n_s > context_lens[s]
  * or context_lens[s] > max_context_len sets the device index flag and is skipped.
- * Tensor cores only: f16/bf16, head_dim 128, query-head groups <= 16, block size 8,
+ * Tensor cores only: f16/bf16, head_dim 64 or 128, query-head groups <= 16, block size 8,
  * 16 or 32, at most 4095 KV heads (else PKV_ERR_UNSUPPORTED); q, out and the pools
  * 16-byte aligned.  workspace: at least paged_attention_prefill_workspace_bytes(...)
  * bytes, 256-byte aligned.

@@ -430,8 +430,8 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d", num_q_heads,
                 cache->num_kv_heads);
   const int group = num_q_heads / cache->num_kv_heads;
-  if (cache->head_dim != 128 || !tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
-    return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 128 and query-head groups <= 16");
+  if (!tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 64 or 128 and query-head groups <= 16");
   if (cache->num_kv_heads > 4095)  // a work-list entry packs the KV head into 12 bits
     return fail(PKV_ERR_UNSUPPORTED, "prefill supports at most 4095 KV heads (%d)", cache->num_kv_heads);
   if (num_query_tokens < 0 || max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
@@ -475,6 +475,7 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
   p.max_context_len = max_context_len;
   p.num_query_tokens = num_query_tokens;
   p.tile_tokens = prefill_tile_tokens(group);
+  p.head_dim = cache->head_dim;
   p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = launch_prefill_tc(p, cache->dtype, static_cast<cudaStream_t>(stream));

@@ -30,20 +30,21 @@ struct DecodeParams {
   float scale_log2;  // softmax scale * log2(e): scores live in the exp2 domain
 };
 
-// Multi-token causal (prefill) attention, tensor cores.
+// Multi-token causal (prefill) attention, tensor cores; f16/bf16, head_dim 64 or 128.
 struct PrefillParams {
-  const void* q;  // [T][Hq][128]
+  const void* q;  // [T][Hq][head_dim]
   const void* k_cache;
   const void* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
   const int32_t* query_start;  // [S+1]
-  void* out;                   // [T][Hq][128]
+  void* out;                   // [T][Hq][head_dim]
   int4* work_list;
   int* work_count;
   int* err;
   int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
   int32_t block_size, num_blocks, max_context_len, num_query_tokens, tile_tokens;
+  int32_t head_dim;  // 64 or 128
   int32_t out_f32;
   float scale_log2;
 };

@@ -1,6 +1,6 @@
 // prefill_tc.cu -- multi-token paged attention with a causal mask (prefill and
-// chunked prefill) on the tcgen05 tensor cores; f16/bf16, head_dim 128, up to 16
-// query heads per KV head.
+// chunked prefill) on the tcgen05 tensor cores; f16/bf16, head_dim 64 or 128, up to
+// 16 query heads per KV head.
 //
 // What it computes ("anthology-of-the-sota note-023", Method: attention gathers K/V
 // through the block table; the same arithmetic as attention over contiguous memory):
@@ -15,8 +15,8 @@
 // the 128-byte swizzled operand layout.  A work item is a PAIR of consecutive tiles of
 // one (sequence, KV head): both consume the same K/V chunks, so each chunk is read once
 // for 256 query rows.  Per 64-key chunk and tile:
-//   S[128 rows x 64 keys] = Q . K^T             (M=128, N=64,  K=128 dims)
-//   O[128 rows x 128 dims] += P . V             (M=128, N=128, K=64 keys), twice:
+//   S[128 rows x 64 keys] = Q . K^T             (M=128, N=64, K=D dims)
+//   O[128 rows x D dims] += P . V               (M=128, N=D,  K=64 keys), twice:
 // the probabilities as hi = round(p) and lo = round(p - hi) in the cache dtype, so the
 // 16-bit operand costs about 2^-17 relative per weight.  S (double-buffered) and O of
 // each tile live in TMEM; the probabilities are written back over the S columns they
@@ -32,7 +32,8 @@
 //  * warps 0-3 and 4-7: one softmax warpgroup per tile of the pair (thread = query
 //    row = TMEM lane); the two groups and the tensor cores work concurrently.
 //  * warp 8, producer: per item the query boxes of both tiles into a double buffer,
-//    then per chunk one 4-D TMA box per block for K and one for V into a 3-stage ring
+//    then per chunk one 4-D TMA box per block for K and one for V into a 48 KB ring
+//    (3 stages at D = 128, 6 at D = 64)
 //    (blocks past the pair's last position come from outside the tensor: zero fill).
 //  * warp 9, MMA: one lane polls four streams -- QK and PV of each tile -- and issues
 //    whatever is ready; a ring stage is released once both tiles' PVs of its chunk are
@@ -55,24 +56,32 @@ constexpr int kThreads = (4 * kGroups + 3) * 32;
 constexpr int kProducerWarp = 4 * kGroups, kMmaWarp = 4 * kGroups + 1, kVWarp = 4 * kGroups + 2;
 constexpr int kRows = 128;                 // query rows per tile (M)
 constexpr int kKC = 64;                    // keys per chunk
-constexpr int kStages = 3;                 // per ring (K and V have one each)
-constexpr int kGroup = 2048;               // 8-row group of a 128-dim tile: two 64-column halves
-constexpr int kKVTile = kKC * 256;         // K (or V) of one chunk: 16 KB
-constexpr int kQBytes = kRows * 256;       // 32 KB per tile: [16 groups][2 halves][8 rows][128 B]
-constexpr int kQItem = kGroups * kQBytes;  // both tiles of an item
-constexpr int kOffV = kStages * kKVTile;
-constexpr int kOffQ = 2 * kStages * kKVTile;
-constexpr int kOffBar = kOffQ + 2 * kQItem;
-// K ring full/empty, V ring full/empty, qfull[2], qempty[2], then per tile: sfull[2],
-// pfull[2], pvdone[2]; drain
-constexpr int kNumBars = 4 * kStages + 4 + kGroups * 6 + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64;
-constexpr uint32_t kTmemCols = 512;        // per tile g: S[2] at 256g + 0/64, O at 256g + 128
+constexpr uint32_t kTmemCols = 512;        // per tile g: S[2] at 256g + 0/64, O at 256g + 128 (D columns)
 constexpr float kRescaleSlack = 8.f;       // log2 units a row's max may grow before O is rescaled
 constexpr int kListThreads = 1024;
 constexpr int kMaxBuckets = 1024;          // chunk-count buckets of the work list (last one open-ended)
-static_assert(kSmemBytes <= 232448, "shared memory");
+
+// Shared-memory layout for head_dim D (64 or 128): K, V and Q tiles as [8-row group]
+// [64-column block][8 rows][128 B], 128-byte swizzled.
+template <int D>
+struct PfLayout {
+  static constexpr int kBlocks = D / 64;                  // 64-column blocks of a row
+  static constexpr int kGroup = 8 * D * 2;                // one 8-row group: all its blocks
+  static constexpr int kKVTile = kKC * D * 2;             // K (or V) of one chunk: 8 or 16 KB
+  static constexpr int kStages = 3 * 128 / D;             // per ring (K and V have one each): 48 KB
+  static constexpr int kQBytes = kRows * D * 2;           // one tile's queries: 16 or 32 KB
+  static constexpr int kQItem = kGroups * kQBytes;        // both tiles of an item
+  static constexpr int kOffV = kStages * kKVTile;
+  static constexpr int kOffQ = 2 * kStages * kKVTile;
+  static constexpr int kOffBar = kOffQ + 2 * kQItem;
+  // K ring full/empty, V ring full/empty, qfull[2], qempty[2], then per tile: sfull[2],
+  // pfull[2], pvdone[2]; drain
+  static constexpr int kNumBars = 4 * kStages + 4 + kGroups * 6 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(kOffQ % 1024 == 0 && kSmemBytes <= 232448, "shared memory");
+};
 
 struct Bars {
   uint64_t *kfull, *kempty, *vfull, *vempty, *qfull, *qempty, *grp, *drain;
@@ -82,8 +91,10 @@ struct Bars {
   __device__ __forceinline__ uint64_t* pvdone(int g, int i) const { return grp + 6 * g + 4 + i; }
 };
 
+template <int D>
 __device__ __forceinline__ Bars carve(unsigned char* smem) {
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  constexpr int kStages = PfLayout<D>::kStages;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + PfLayout<D>::kOffBar);
   Bars r;
   r.kfull = b;
   r.kempty = b + kStages;
@@ -99,7 +110,7 @@ __device__ __forceinline__ Bars carve(unsigned char* smem) {
 struct PrefillArgs {
   CUtensorMap tk;  // pool 4-D views: one box = one block's tile for one KV head
   CUtensorMap tv;
-  CUtensorMap tq;  // queries (128 dims, heads, tokens): one box = 8 tokens x 64 dims of one head
+  CUtensorMap tq;  // queries (head_dim, heads, tokens): one box = 8 tokens x 64 dims of one head
   PrefillParams p;
 };
 
@@ -144,9 +155,11 @@ __device__ __forceinline__ float chunk_extreme(float* sv, bool diagonal, int lim
 // One producer warp's copies of an item's chunks of K (or V) into its ring: per chunk
 // one 4-D box per block (blocks past the pair's last position from outside the tensor:
 // zero fill).  `c` counts the warp's chunks over all items.  Returns false on abort.
+template <int D>
 __device__ __forceinline__ bool load_chunks(const PrefillParams& p, const Item& it, const CUtensorMap* map,
                                             unsigned char* ring, uint64_t* full, uint64_t* empty, int& c,
                                             int* issued_slot, uint64_t policy, volatile int* abort_flag) {
+  constexpr int kStages = PfLayout<D>::kStages, kKVTile = PfLayout<D>::kKVTile;
   const int lane = threadIdx.x % 32;
   const int bs = p.block_size;
   const int blocks_per_chunk = kKC / bs;
@@ -173,19 +186,23 @@ __device__ __forceinline__ bool load_chunks(const PrefillParams& p, const Item& 
         }
         grp = (b * p.num_kv_heads + it.g) * bs / 8;
       }
-      tma_load_4d(ring + st * kKVTile + lane * bs * 256, map, grp, &full[st], policy);
+      tma_load_4d(ring + st * kKVTile + lane * bs * (D * 2), map, grp, &full[st], policy);
     }
     if (lane == 0) *issued_slot = c + 1;
   }
   return true;
 }
 
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+  using L = PfLayout<D>;
+  constexpr int kStages = L::kStages, kGroup = L::kGroup, kKVTile = L::kKVTile;
+  constexpr int kQBytes = L::kQBytes, kQItem = L::kQItem, kOffV = L::kOffV, kOffQ = L::kOffQ;
+  constexpr int kOffMisc = L::kOffMisc;
   extern __shared__ __align__(1024) unsigned char smem[];
   const PrefillParams& p = a.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Bars bars = carve(smem);
+  const Bars bars = carve<D>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* kissued_slot = reinterpret_cast<int*>(smem + kOffMisc + 8);
@@ -232,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     const uint64_t pol_kv = policy_evict_normal();  // K/V: re-read by the sequence's other items
     const uint64_t pol_q = policy_evict_first();    // Q: read once
-    // this lane's query box of a tile: 8-row group lane / 2, half lane % 2
-    const int qrows = (lane >> 1) * 8, qhalf = lane & 1;
+    // this lane's query box of a tile: 8-row group lane / kBlocks, 64-column block lane % kBlocks
+    const int qrows = (lane / L::kBlocks) * 8, qhalf = lane % L::kBlocks;
     const int qhead = qrows / TQ, qtok = qrows % TQ;
     int c = 0, j = 0;
     bool ok = true;
@@ -249,17 +266,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
+      if (lane < 16 * L::kBlocks) {
 #pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        // padding groups (past the G heads) read tokens outside the tensor: zeros
-        const int tok = qhead < G ? it.qrow0 + g * TQ + qtok : p.num_query_tokens;
-        const int head = it.g * G + min(qhead, G - 1);
-        tma_load_3d(smem + kOffQ + qb * kQItem + g * kQBytes + (lane >> 1) * kGroup + qhalf * 1024, &a.tq,
-                    qhalf * 64, head, tok, &bars.qfull[qb], pol_q);
+        for (int g = 0; g < kGroups; ++g) {
+          // padding groups (past the G heads) read tokens outside the tensor: zeros
+          const int tok = qhead < G ? it.qrow0 + g * TQ + qtok : p.num_query_tokens;
+          const int head = it.g * G + min(qhead, G - 1);
+          tma_load_3d(smem + kOffQ + qb * kQItem + g * kQBytes + (lane / L::kBlocks) * kGroup + qhalf * 1024, &a.tq,
+                      qhalf * 64, head, tok, &bars.qfull[qb], pol_q);
+        }
       }
       if (lane == 0) *qissued_slot = j + 1;
       // ---- K chunks (a stage is free once both tiles' QKs of its chunk completed) ----
-      ok = load_chunks(p, it, &a.tk, smem, bars.kfull, bars.kempty, c, kissued_slot, pol_kv, abort_flag);
+      ok = load_chunks<D>(p, it, &a.tk, smem, bars.kfull, bars.kempty, c, kissued_slot, pol_kv, abort_flag);
     }
   } else if (warp == kVWarp) {
     // ============================ producer: V ============================
@@ -270,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     ItemCursor cur;
     for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
       // a stage is free once both tiles' PVs of its chunk completed
-      ok = load_chunks(p, unpack_item(cur.cur, TQ), &a.tv, smem + kOffV, bars.vfull, bars.vempty, c, vissued_slot,
-                       pol_kv, abort_flag);
+      ok = load_chunks<D>(p, unpack_item(cur.cur, TQ), &a.tv, smem + kOffV, bars.vfull, bars.vempty, c,
+                          vissued_slot, pol_kv, abort_flag);
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ============================
@@ -281,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // uniform registers); one elected lane issues.
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kRows, kKC);
-    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, false, true, kRows, 128);
+    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, false, true, kRows, D);
     // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
     const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, kGroup, kLayoutSwizzle128);
     const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroup, kLayoutSwizzle128);
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint64_t dq = dqb + ((g * kQBytes) >> 4);
           const uint32_t d = tmem + g * 256 + sb * 64;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
             mma_f16(d, dq + off, dk + off, idesc_qk, kk > 0);
           }
@@ -407,17 +426,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       tc_fence_after();
       const float inv = 1.f / lsum;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < D / 32; ++q) {
         float o[32];
         tmem_load32(obuf + q * 32, o);
         if (row >= 0) {
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(row) * 128 + q * 32);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + static_cast<size_t>(row) * D + q * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + static_cast<size_t>(row) * 128 + q * 32);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + static_cast<size_t>(row) * D + q * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pack2<T>(o[8 * i] * inv, o[8 * i + 1] * inv),
@@ -481,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < D / 16; ++q) {
             float o[16];
             tmem_load16(obuf + q * 16, o);
 #pragma unroll
@@ -530,10 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (t >= rows_needed && t < rows_loaded) {
             unsigned char* vrow = smem + kOffV + (c % kStages) * kKVTile + (t >> 3) * kGroup + (t & 7) * 128;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              reinterpret_cast<uint4*>(vrow)[q] = make_uint4(0, 0, 0, 0);
-              reinterpret_cast<uint4*>(vrow + 1024)[q] = make_uint4(0, 0, 0, 0);
-            }
+            for (int q = 0; q < 8 * L::kBlocks; ++q)  // 128 bytes per 64-column block, 1 KB apart
+              reinterpret_cast<uint4*>(vrow + (q >> 3) * 1024)[q & 7] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
         }
@@ -619,13 +636,14 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
   }
 }
 
-// Queries [tokens][heads][128] seen as 3-D (128 dims, heads, tokens); a box is 8
-// tokens x 64 dims of one head, landing as one swizzled 8-row group half.
-bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16) {
+// Queries [tokens][heads][head_dim] seen as 3-D (head_dim, heads, tokens); a box is 8
+// tokens x 64 dims of one head, landing as one swizzled 64-column block of an 8-row group.
+bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16, int head_dim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {128, heads, tokens};
-  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
+  const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), heads, tokens};
+  cuuint64_t strides[2] = {row, static_cast<cuuint64_t>(heads) * row};
   cuuint32_t box[3] = {64, 1, 8};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q),
@@ -633,16 +651,16 @@ bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t toke
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t launch_prefill_t(const PrefillArgs& args, int grid, cudaStream_t stream) {
+  constexpr int smem = PfLayout<D>::kSmemBytes;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  prefill_tc_kernel<T><<<grid, kThreads, kSmemBytes, stream>>>(args);
+  prefill_tc_kernel<T, D><<<grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 
@@ -662,9 +680,10 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t st
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, 128) ||
-      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, 128) ||
-      !make_query_map(&args.tq, p.q, p.num_q_heads, p.num_query_tokens, bf16))
+  if (p.head_dim != 64 && p.head_dim != 128) return cudaErrorInvalidValue;
+  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
+      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
+      !make_query_map(&args.tq, p.q, p.num_q_heads, p.num_query_tokens, bf16, p.head_dim))
     return cudaErrorInvalidValue;
   prefill_list_kernel<<<1, kListThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -674,7 +693,9 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int dtype, cudaStream_t st
   const size_t items = prefill_max_items(p.num_seqs, p.num_query_tokens, p.num_kv_heads, p.group);
   const int grid = static_cast<int>(items < static_cast<size_t>(sms) ? items : sms);
   if (grid == 0) return cudaSuccess;
-  return bf16 ? launch_prefill_t<__nv_bfloat16>(args, grid, stream) : launch_prefill_t<__half>(args, grid, stream);
+  if (p.head_dim == 64)
+    return bf16 ? launch_prefill_t<__nv_bfloat16, 64>(args, grid, stream) : launch_prefill_t<__half, 64>(args, grid, stream);
+  return bf16 ? launch_prefill_t<__nv_bfloat16, 128>(args, grid, stream) : launch_prefill_t<__half, 128>(args, grid, stream);
 }
 
 }  // namespace pkv

@@ -154,7 +154,7 @@ def test_prefill_argument_checks_before_device_work(lib):
     need = lib.paged_attention_prefill_workspace_bytes(4, 64, 100, ctypes.byref(d))
     assert need > 256
     assert run(_desc(dtype=pkv.F32)) == 2                       # f32 has no prefill path
-    assert run(_desc(head_dim=64)) == 2
+    assert run(_desc(head_dim=96)) == 2                          # head_dim outside {64, 128}
     assert run(d, Hq=8 * 17) == 2                               # group 17
     assert run(_desc(num_kv_heads=4096), Hq=4096) == 2           # KV head packed in 12 bits
     assert b"4095" in lib.paged_kv_last_error()

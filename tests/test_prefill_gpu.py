@@ -20,6 +20,11 @@ CASES = [
     # query-head groups that do not divide 16: 5, 6 and 7 heads per KV head
     ("bf16", 16, 40, 8, 800, 1, None), ("f16", 16, 12, 2, 600, 100, None), ("bf16", 32, 28, 4, 900, 200, None),
 ]
+# head_dim 64: dtype, bs, Hq, Hkv, max_len, min_len, new tokens
+CASES_D64 = [
+    ("bf16", 16, 32, 8, 900, 1, None), ("f16", 8, 16, 1, 700, 300, None), ("bf16", 32, 12, 4, 1500, 1, None),
+    ("f16", 16, 8, 8, 2000, 1200, lambda s, L: 64), ("bf16", 16, 64, 4, 600, 1, lambda s, L: L),
+]
 
 
 def run(w, q, qs, out_dtype=torch.float32):
@@ -38,6 +43,24 @@ def test_prefill_parity(case):
     dt, bs, Hq, Hkv, max_len, min_len, nt = case
     w, q, qs = workloads.prefill_workload(310_900 + CASES.index(case), num_seqs=6, max_len=max_len, min_len=min_len,
                                           num_q_heads=Hq, num_kv_heads=Hkv, block_size=bs, dtype=dt, new_tokens=nt)
+    if int(qs[-1]) == 0:
+        pytest.skip("no new tokens")
+    ref = oracle.attention_prefill(q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, qs, w.scale)
+    out = run(w, q, qs)
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= 2e-3, f"max-abs {err:.3g}"
+    low = run(w, q, qs, w.dtype)
+    assert torch.equal(low.cpu().view(torch.uint8), out.to(w.dtype).cpu().view(torch.uint8))
+
+
+@pytest.mark.parametrize("case", CASES_D64, ids=[f"{c[0]}-bs{c[1]}-{c[2]}x{c[3]}-L{c[4]}" for c in CASES_D64])
+def test_prefill_parity_head_dim_64(case):
+    dt, bs, Hq, Hkv, max_len, min_len, nt = case
+    w, q, qs = workloads.prefill_workload(310_940 + CASES_D64.index(case), num_seqs=6, max_len=max_len,
+                                          min_len=min_len, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=64,
+                                          block_size=bs, dtype=dt, new_tokens=nt)
     if int(qs[-1]) == 0:
         pytest.skip("no new tokens")
     ref = oracle.attention_prefill(q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, qs, w.scale)
