@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true", help="measure causal multi-token (prefill) attention instead")
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size (8/16/32)")
+    ap.add_argument("--head-dim", type=int, default=0, help="override the workload's head_dim (64/128)")
+    ap.add_argument("--num-q-heads", type=int, default=0,
+                    help="override the workload's query heads (a multiple of its KV heads: another group size)")
     ap.add_argument("--identity-tables", action="store_true",
                     help="physical blocks in logical order (contiguous sequences): the indirection A/B")
     return ap.parse_args()
@@ -411,7 +414,8 @@ def main():
 
     path = {"auto": pkv.PATH_AUTO, "cuda_core": pkv.PATH_CUDA_CORE, "tensor_core": pkv.PATH_TENSOR_CORE}[args.path]
     # every rank decodes its own batch of the same workload shape (independent replicas)
-    overrides = {"block_size": args.block_size} if args.block_size else {}
+    overrides = {k: v for k, v in (("block_size", args.block_size), ("head_dim", args.head_dim),
+                                   ("num_q_heads", args.num_q_heads)) if v}
     w = workloads.make_workload(args.config, canary=False, pool_device=dev, shuffle=not args.identity_tables,
                                 **overrides)
     g = w.to(dev)

@@ -203,7 +203,12 @@ def make_workload(config: int, *, canary: bool = True, pool_device="cpu", shuffl
     seed = SEED_BASE + config
     g = torch.Generator().manual_seed(seed)
     bs = c["block_size"]
-    common = dict(name=c["name"], seed=seed, dtype=c["dtype"], num_q_heads=c["num_q_heads"],
+    # a workload with fields changed is named as such (its figures are not the base one's)
+    changed = {k: v for k, v in sorted(overrides.items()) if CONFIGS[config].get(k) != v}
+    name = c["name"]
+    if changed:
+        name += " [with " + ", ".join(f"{k}={v}" for k, v in changed.items()) + "]"
+    common = dict(name=name, seed=seed, dtype=c["dtype"], num_q_heads=c["num_q_heads"],
                   num_kv_heads=c["num_kv_heads"], head_dim=c["head_dim"], block_size=bs,
                   canary=canary, pool_device=pool_device, gen=g, shuffle=shuffle)
     kind = c["kind"]
