@@ -48,7 +48,7 @@
  *    runs out, sets a device flag, skips the access and completes;
  *    paged_kv_device_error() reports and clears that flag.
  *  - Supported set: dtype f32, f16, bf16 (q, k, v, caches share it); out dtype
- *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16 or 32;
+ *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
  *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
  *    up to 8 on the CUDA-core decode path and up to 16 on the tensor-core paths
  *    (f16/bf16, head_dim 64 or 128).
@@ -79,7 +79,7 @@ typedef enum {
 /* Geometry of one layer's block pool (both k_cache and v_cache). */
 typedef struct {
   int32_t num_blocks;   /* physical blocks in the pool */
-  int32_t block_size;   /* tokens per block: 8, 16 or 32 */
+  int32_t block_size;   /* tokens per block: 8, 16, 32 or 64 */
   int32_t num_kv_heads;
   int32_t head_dim;     /* 64 or 128 */
   int32_t dtype;        /* pkv_dtype of the caches, q, k and v */
@@ -250,7 +250,7 @@ size_t paged_attention_no_alloc_limit(void);
  * query_start[num_seqs] = num_query_tokens.  A sequence with n_s > context_lens[s]
  * or context_lens[s] > max_context_len sets the device index flag and is skipped.
  * Tensor cores only: f16/bf16, head_dim 64 or 128, query-head groups <= 16, block size 8,
- * 16 or 32, at most 4095 KV heads (else PKV_ERR_UNSUPPORTED); q, out and the pools
+ * 16, 32 or 64, at most 4095 KV heads (else PKV_ERR_UNSUPPORTED); q, out and the pools
  * 16-byte aligned.  workspace: at least paged_attention_prefill_workspace_bytes(...)
  * bytes, 256-byte aligned.
  */

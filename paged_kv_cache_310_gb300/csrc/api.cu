@@ -64,8 +64,8 @@ pkv_status check_cache(const pkv_cache_desc* c) {
   if (c->num_blocks <= 0 || c->num_kv_heads <= 0)
     return fail(PKV_ERR_INVALID_ARG, "num_blocks %d, num_kv_heads %d must be positive",
                 c->num_blocks, c->num_kv_heads);
-  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
-    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", c->block_size);
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32 && c->block_size != 64)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32, 64)", c->block_size);
   if (c->head_dim != 64 && c->head_dim != 128)
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
   if (c->num_kv_heads > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d", c->num_kv_heads);

@@ -142,8 +142,10 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     if (lane == 0) {
       const size_t tile_elems = static_cast<size_t>(bs) * D;
       const size_t block_stride = static_cast<size_t>(p.num_kv_heads) * tile_elems;
-      const uint32_t tile_bytes = static_cast<uint32_t>(bs) * C::kRowBytes;
-      const int blocks_per_chunk = C::kChunk / bs;
+      // one bulk copy per block of a stage, or per stage-sized piece of a block when a
+      // block (64 tokens) spans several stages: its rows are contiguous either way
+      const int copy_rows = bs < C::kChunk ? bs : C::kChunk;
+      const uint32_t copy_bytes = static_cast<uint32_t>(copy_rows) * C::kRowBytes;
       const uint64_t policy = policy_evict_first();  // K/V are streamed once
       int issued = 0;
       for (int c = 0; c < nchunks; ++c) {
@@ -155,15 +157,16 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
         }
         if (*reinterpret_cast<volatile int*>(&flags[0]) != INT_MAX) break;
         const int rows = min(C::kChunk, ntok - c * C::kChunk);
-        const int nb = (rows + bs - 1) / bs;
+        const int ncopies = (rows + copy_rows - 1) / copy_rows;
         unsigned char* kdst = ring + st * C::kStageBytes;
         unsigned char* vdst = kdst + C::kChunk * C::kRowBytes;
-        mbar_arrive_expect_tx(&full[st], 2u * nb * tile_bytes);
-        for (int i = 0; i < nb; ++i) {
-          const size_t off = ids[c * blocks_per_chunk + i] * block_stride + g * tile_elems;
-          bulk_load_hint(kdst + i * tile_bytes, static_cast<const T*>(p.k_cache) + off, tile_bytes,
+        mbar_arrive_expect_tx(&full[st], 2u * ncopies * copy_bytes);
+        for (int i = 0; i < ncopies; ++i) {
+          const int tok = c * C::kChunk + i * copy_rows;  // first token of the piece, partition-relative
+          const size_t off = ids[tok / bs] * block_stride + g * tile_elems + static_cast<size_t>(tok % bs) * D;
+          bulk_load_hint(kdst + i * copy_bytes, static_cast<const T*>(p.k_cache) + off, copy_bytes,
                          &full[st], policy);
-          bulk_load_hint(vdst + i * tile_bytes, static_cast<const T*>(p.v_cache) + off, tile_bytes,
+          bulk_load_hint(vdst + i * copy_bytes, static_cast<const T*>(p.v_cache) + off, copy_bytes,
                          &full[st], policy);
         }
         issued = c + 1;

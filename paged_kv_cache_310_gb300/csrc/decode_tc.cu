@@ -790,7 +790,7 @@ cudaError_t launch_tc_d(const TcArgs& args, int grid, cudaStream_t stream) {
 bool tc_supported(int dtype, int head_dim, int group, int block_size) {
   return (dtype == PKV_F16 || dtype == PKV_BF16) && (head_dim == 64 || head_dim == 128) && group >= 1 &&
          group <= kN &&
-         (block_size == 8 || block_size == 16 || block_size == 32);
+         (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream) {

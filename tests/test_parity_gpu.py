@@ -140,6 +140,9 @@ CASES = [
     ("f16", 128, 32, 4, 4, 200, 0), ("bf16", 128, 8, 24, 8, 3000, 384),
     ("f32", 128, 32, 3, 3, 1100, 0), ("f16", 64, 16, 4, 2, 2100, 256), ("bf16", 64, 8, 8, 1, 777, 384),
     ("bf16", 64, 16, 32, 2, 1800, 512), ("f16", 64, 32, 12, 1, 600, 0),
+    # 64-token blocks: a block spans two CUDA-core stages and half a tensor-core chunk
+    ("bf16", 128, 64, 16, 4, 1500, 0), ("f16", 64, 64, 8, 8, 700, 256), ("f32", 128, 64, 4, 2, 900, 128),
+    ("bf16", 128, 64, 8, 1, 130, 128), ("f32", 64, 64, 2, 2, 2500, 0),
 ]
 
 

@@ -19,11 +19,14 @@ CASES = [
     ("bf16", 8, 4, 4, 3000, 2000, lambda s, L: L),
     # query-head groups that do not divide 16: 5, 6 and 7 heads per KV head
     ("bf16", 16, 40, 8, 800, 1, None), ("f16", 16, 12, 2, 600, 100, None), ("bf16", 32, 28, 4, 900, 200, None),
+    # 64-token blocks: one block per 64-key chunk
+    ("bf16", 64, 32, 8, 1200, 1, None), ("f16", 64, 8, 1, 900, 400, lambda s, L: 100),
 ]
 # head_dim 64: dtype, bs, Hq, Hkv, max_len, min_len, new tokens
 CASES_D64 = [
     ("bf16", 16, 32, 8, 900, 1, None), ("f16", 8, 16, 1, 700, 300, None), ("bf16", 32, 12, 4, 1500, 1, None),
     ("f16", 16, 8, 8, 2000, 1200, lambda s, L: 64), ("bf16", 16, 64, 4, 600, 1, lambda s, L: L),
+    ("bf16", 64, 16, 2, 1000, 1, None),
 ]
 
 
