@@ -232,4 +232,45 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
+// Sums each of N values over aligned groups of LANES lanes (N <= LANES, both powers of
+// two) and leaves all N totals in every lane of the group: a reduce-scatter (each step
+// a lane keeps half of its values and adds its partner's copy of that half), a
+// butterfly over the remaining lane bits, then each total fetched from a lane that
+// holds it.  N - 1 + log2(LANES / N) + N shuffles instead of N log2(LANES).
+template <int N, int LANES>
+__device__ __forceinline__ void group_sum_all(float (&v)[N]) {
+  static_assert(N <= LANES && LANES <= 32, "at most one value per lane of the group");
+  if (N == 1) {
+    v[0] = group_sum<LANES>(v[0]);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  float a[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) a[i] = v[i];
+  int off = LANES / 2;
+#pragma unroll
+  for (int n = N; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = lane & off;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? a[i] : a[i + n / 2];
+      const float keep = upper ? a[i + n / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float r = a[0];
+#pragma unroll
+  for (; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  // the lane of the group holding total j: j's binary digits, most significant first,
+  // on the lane bits LANES/2, LANES/4, ... (a compile-time index within the group)
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    int src = 0;
+#pragma unroll
+    for (int b = N / 2, o = LANES / 2; b > 0; b >>= 1, o >>= 1) src += (j & b) ? o : 0;
+    v[j] = __shfl_sync(0xffffffffu, r, src, LANES);
+  }
+}
+
 }  // namespace pkv

@@ -220,15 +220,19 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int e = 0; e < C::kVec; ++e) kf[e] = 0.f;
         }
+        float d[GM];
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
           float2 d2 = make_float2(0.f, 0.f);  // even and odd elements: two short chains
 #pragma unroll
           for (int e = 0; e < C::kVec; e += 2)
             d2 = __ffma2_rn(make_float2(qf[h][e], qf[h][e + 1]), make_float2(kf[e], kf[e + 1]), d2);
-          float d = group_sum<C::kLanesPerRow>(d2.x + d2.y);
-          sc[i][h] = valid ? d : -INFINITY;
+          d[h] = d2.x + d2.y;
         }
+        // the GM dot products over the row's lanes at once (fewer shuffles than one by one)
+        group_sum_all<GM, C::kLanesPerRow>(d);
+#pragma unroll
+        for (int h = 0; h < GM; ++h) sc[i][h] = valid ? d[h] : -INFINITY;
       }
 #pragma unroll
       for (int h = 0; h < GM; ++h) {
