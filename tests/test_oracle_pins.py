@@ -155,12 +155,13 @@ def test_bruteforce_config1():
 # --------------------------------------------------------------------------------------
 # identity block table == plain attention on a contiguous buffer (library softmax)
 
-@pytest.mark.parametrize("G", [1, 4])
-def test_identity_table_matches_library_attention(G):
+@pytest.mark.parametrize("G,bs,M,lens", [(1, 4, 6, [5, 24, 13]), (4, 4, 6, [5, 24, 13]), (2, 64, 3, [5, 130, 64])],
+                         ids=["G1-bs4", "G4-bs4", "G2-bs64"])
+def test_identity_table_matches_library_attention(G, bs, M, lens):
     gen = torch.Generator().manual_seed(310_201)
-    S, Hkv, D, bs, M = 3, 2, 16, 4, 6
+    S, Hkv, D = 3, 2, 16
     Hq = Hkv * G
-    lens = torch.tensor([5, 24, 13], dtype=torch.int32)
+    lens = torch.tensor(lens, dtype=torch.int32)
     kc = torch.randn(S * M, Hkv, bs, D, generator=gen, dtype=torch.float64).float()
     vc = torch.randn(S * M, Hkv, bs, D, generator=gen, dtype=torch.float64).float()
     q = torch.randn(S, Hq, D, generator=gen).float()
