@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true", help="measure causal multi-token (prefill) attention instead")
-    ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size (8/16/32)")
+    ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size (8/16/32/64)")
     ap.add_argument("--head-dim", type=int, default=0, help="override the workload's head_dim (64/128)")
     ap.add_argument("--num-q-heads", type=int, default=0,
                     help="override the workload's query heads (a multiple of its KV heads: another group size)")

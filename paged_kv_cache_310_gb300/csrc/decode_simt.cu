@@ -14,14 +14,16 @@
 //  * warp 4 is the producer: it stages the partition's block ids in shared memory,
 //    then one lane streams the partition through a 3- or 4-stage ring.  A stage holds
 //    32 tokens: one 1-D bulk copy (TMA engine, cp.async.bulk) per (block, kv head) tile
-//    for K and one for V; each tile is block_size*head_dim contiguous elements.
-//    Completion is counted in bytes on the stage's "full" mbarrier.
+//    for K and one for V (each tile is block_size*head_dim contiguous elements; a
+//    64-token block spans two stages and is copied half per stage).  Completion is
+//    counted in bytes on the stage's "full" mbarrier.
 //  * warps 0-3 consume.  A row of head_dim elements is spread over head_dim/vec lanes
 //    (16-byte vectors), so a warp covers 32/(lanes per row) rows at once; each such
 //    lane group ("slot") owns the rows r == slot (mod slots) of every stage and keeps
 //    its own running max / sum / output per query head (online softmax, exp2 domain).
-//    Scores are warp-shuffle reductions; after a stage the warp arrives on the
-//    stage's "empty" mbarrier so the producer can refill it.
+//    A row's G dot products are all-reduced over its lanes together (warp shuffles);
+//    after a stage the warp arrives on the stage's "empty" mbarrier so the producer
+//    can refill it.
 //  * at the end the slots are combined through shared memory in a fixed order, so
 //    the result depends only on logical token positions (bit-identical under any
 //    placement of the physical blocks).
@@ -29,7 +31,6 @@
 //  writes (max, sum, un-normalised output) to the workspace and merge_kernel
 //  combines them: M = max_p m_p, out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
 #include <climits>
-
 
 #include "common.cuh"
 #include "launch.h"

@@ -23,25 +23,26 @@
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
 // head) that work_list_kernel sorts longest first and the CTAs take in snake order;
 // the kernel is launched as a programmatic dependent of that list kernel.  224 threads
-// in five roles:
+// (352 from 4 query heads per KV head) in five roles:
 //  * warp 4, producer of Q and K: per 128-token chunk, one lane per physical block
 //    reads the block id (before waiting for a free stage, hiding its latency) and
 //    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
 //    128-byte swizzle) into a 96 KB K ring (3 stages at D = 128, 6 at D = 64); blocks
 //    past the item's end are loaded from outside the tensor, which the TMA unit fills
-//    with zeros.  It also loads the
-//    item's 16 query rows.
-//  * warp 6, producer of V: the same for V tiles into a V ring of the same size.  The rings are
-//    separate so that a K stage is reused as soon as its chunk's QK completes, long
-//    before the chunk's V is done with: more of the rings stays in flight, and the
-//    kernel is bound by bytes in flight.
+//    with zeros.  It also loads the item's 16 query rows.
+//  * warp 6, producer of V: the same for V tiles into a V ring of the same size.  The
+//    rings are separate so that a K stage is reused as soon as its chunk's QK
+//    completes, long before the chunk's V is done with: more of the rings stays in
+//    flight, and the kernel is bound by bytes in flight.
 //  * warp 5, MMA: the whole warp polls (one batched barrier probe per round) and an
 //    elected lane issues PV for the oldest chunk whose probabilities are in shared
 //    memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed; commits
 //    release the ring stages and signal the softmax warps.
-//  * warps 0-3, softmax (thread t = TMEM lane t): read S row t (token t, 16 heads),
-//    vote on whether any score exceeds its head's running max by more than 2^8 (if
-//    so, chunk max across the 128 tokens by shuffles + shared memory and an
+//  * warps 0-3, and from G = 4 also warps 7-10, softmax (thread t = TMEM lane t; a warp
+//    reads the lane quarter of its index mod 4, so with eight warps two share each
+//    quarter and take half of the heads each): read S row t (token t, its heads), vote
+//    on whether any score exceeds its head's running max by more than 2^8 (if so,
+//    chunk max across the 128 tokens by a warp reduction + shared memory and an
 //    online-softmax rescale), probabilities split into two parts rounded to the cache
 //    dtype (hi = round(p), lo = round(p - hi)) into P^T (shared memory), then read O
 //    row t (dimension t) of the previous chunk, add its hi and lo columns and

@@ -26,20 +26,24 @@
 // brings a score more than 8 (log2 units) above it -- probabilities stay <= 256 -- and
 // only then is its O row rescaled in TMEM.
 //
-// Roles (320 threads, persistent CTAs over a work list in which a sequence's items are
+// Roles (352 threads, persistent CTAs over a work list in which a sequence's items are
 // adjacent -- they share K/V, which then stays in L2 -- and sequences come longest
 // first, dealt in snake order):
 //  * warps 0-3 and 4-7: one softmax warpgroup per tile of the pair (thread = query
 //    row = TMEM lane); the two groups and the tensor cores work concurrently.
-//  * warp 8, producer: per item the query boxes of both tiles into a double buffer,
-//    then per chunk one 4-D TMA box per block for K and one for V into a 48 KB ring
-//    (3 stages at D = 128, 6 at D = 64)
-//    (blocks past the pair's last position come from outside the tensor: zero fill).
-//  * warp 9, MMA: one lane polls four streams -- QK and PV of each tile -- and issues
-//    whatever is ready; a ring stage is released once both tiles' PVs of its chunk are
-//    issued (their commit fires when they complete).  tcgen05 MMAs of one thread run
-//    in issue order, so QK(c + 2) may overwrite the probabilities of chunk c once
-//    PV(c) has been issued.
+//  * warp 8, producer of Q and K: per item the query boxes of both tiles into a double
+//    buffer, then per chunk one 4-D TMA box per block of K into a 48 KB ring (3 stages
+//    at D = 128, 6 at D = 64; blocks past the pair's last position come from outside
+//    the tensor: zero fill).  A K stage is free once both tiles' QKs of its chunk
+//    completed.
+//  * warp 10, producer of V: the same for V into its own ring, whose stage is free once
+//    both tiles' PVs of its chunk completed.
+//  * warp 9, MMA: a fixed schedule per chunk c -- PV of tile 0, PV of tile 1, then QK
+//    of both tiles for chunk c + 2, whose S columns held the probabilities of chunk c
+//    (tcgen05 MMAs of one thread run in issue order, so that QK may overwrite them
+//    once PV(c) has been issued).  The whole warp runs it with warp-uniform control
+//    flow; one batched barrier probe per chunk covers everything it needs, and one
+//    elected lane issues.
 #include <climits>
 #include <type_traits>
 
