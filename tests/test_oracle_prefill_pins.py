@@ -43,8 +43,9 @@ def test_one_new_token_is_decode():
 
 @pytest.mark.parametrize("seed", range(5))
 def test_prefill_bruteforce(seed):
-    # the last case has 64-token blocks, contexts spanning up to three of them
-    w, kc, vc, q, qs = _case(310_810 + seed, dtype=["f32", "bf16", "f16", "bf16", "f16"][seed],
+    # the last case has 64-token blocks, contexts of 146 and 103 tokens (three and two)
+    w, kc, vc, q, qs = _case([310_810, 310_811, 310_812, 310_813, 310_821][seed],
+                             dtype=["f32", "bf16", "f16", "bf16", "f16"][seed],
                              Hq=[2, 4, 4, 8, 4][seed], Hkv=[2, 1, 2, 2, 2][seed], S=[3, 3, 3, 3, 2][seed],
                              max_ctx=[70, 70, 70, 70, 150][seed], bs=[8, 8, 8, 8, 64][seed])
     got = oracle.attention_prefill(q, kc, vc, w.block_tables, w.context_lens, qs, w.scale)
