@@ -139,6 +139,18 @@ def test_plan_reports_path_partitions_and_launches(lib):
     assert pkv.paged_attention_plan(64, 8, 2048, k16)["path"] == pkv.PATH_TENSOR_CORE  # automatic, bf16 D128
     k32 = __import__("torch").empty((1, 8, 16, 64), dtype=__import__("torch").float32)
     assert pkv.paged_attention_plan(64, 8, 2048, k32)["path"] == pkv.PATH_CUDA_CORE   # f32, D64
+    torch = __import__("torch")
+    k16d64 = torch.empty((1, 8, 16, 64), dtype=torch.float16)
+    assert pkv.paged_attention_plan(64, 8, 2048, k16d64)["path"] == pkv.PATH_TENSOR_CORE  # f16, D64
+    k16b64 = torch.empty((1, 8, 64, 128), dtype=torch.bfloat16)
+    assert pkv.paged_attention_plan(128, 8, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # 64-token blocks
+    k32b64 = torch.empty((1, 8, 64, 128), dtype=torch.float32)
+    assert pkv.paged_attention_plan(32, 8, 2048, k32b64)["path"] == pkv.PATH_CUDA_CORE
+    with pytest.raises(pkv.PagedKVError):   # f32 has no tensor-core path
+        pkv.paged_attention_plan(64, 8, 2048, k32, path=pkv.PATH_TENSOR_CORE)
+    with pytest.raises(pkv.PagedKVError):   # f32 at group 16: above the CUDA-core path's 8
+        pkv.paged_attention_plan(4, 128, 2048, k32b64)
+    assert pkv.paged_attention_plan(4, 128, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # bf16 at group 16
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_attention_plan(64, 8, 2048, k16, path=pkv.PATH_TENSOR_CORE, partition_tokens=8192)
 
