@@ -54,6 +54,8 @@ def parse():
                     help="override the workload's query heads (a multiple of its KV heads: another group size)")
     ap.add_argument("--identity-tables", action="store_true",
                     help="physical blocks in logical order (contiguous sequences): the indirection A/B")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the decode-call timing of workloads 3, 4 and 5 on the default line")
     return ap.parse_args()
 
 
@@ -158,6 +160,72 @@ class ClockSampler:
         loaded = [x for x in sm if mx and x >= 0.5 * max(mx)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+DECODE_CALLS_MIN = 200
+
+
+def decode_call_ms(call, stream, n):
+    """Mean device time of one decode call: each of n calls bracketed by CUDA events
+    on the stream it is launched on."""
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        k0[i].record(stream)
+        call()
+        k1[i].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in zip(k0, k1))
+
+
+def measure_config(pkv, cfg, dev, path, partition, n_calls):
+    """Decode-call roofline of workload `cfg` (its step's copies and append done once
+    first, as the step does), inputs resident in HBM."""
+    w = workloads.make_workload(cfg, canary=False, pool_device=dev)
+    g = w.to(dev)
+    S, Hq, D = g.q.shape
+    out = torch.empty((S, Hq, D), dtype=w.dtype, device=dev)
+    maxL = w.max_context_len
+    stream = torch.cuda.current_stream(dev)
+    if g.cow_pairs.numel():
+        pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache, host_pairs=w.cow_pairs.cpu())
+    pkv.paged_kv_append(g.k_new, g.v_new, g.slot_mapping, g.k_cache, g.v_cache)
+
+    def call():
+        pkv.paged_attention_decode(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, w.scale, out,
+                                   max_context_len=maxL, path=path, partition_tokens=partition)
+
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    if pkv.device_error() != 0:
+        raise SystemExit(f"device error flag set on workload {cfg}")
+    ms = decode_call_ms(call, stream, n_calls)
+    if pkv.device_error() != 0:
+        raise SystemExit(f"device error flag set on workload {cfg}")
+    plan = pkv.paged_attention_plan(S, Hq, maxL, g.k_cache, path=path, partition_tokens=partition)
+    path_name = {1: "cuda_core", 2: "tensor_core"}[plan["path"]]
+    kv, algo = roofline_bytes(w, elem(out.dtype))
+    peak, peak_kind = peaks()
+    achieved = algo / (ms * 1e-3) / 1e9
+    entry = {"workload": w.name, "path": path_name, "partition_tokens": plan["partition_tokens"],
+             "partitions": plan["max_partitions"], "calls": n_calls, "ms_per_call": ms,
+             "kv_gbs": kv / (ms * 1e-3) / 1e9, "seq_tokens_per_s": int(w.context_lens.sum()) / (ms * 1e-3),
+             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "peak_source": peak_kind,
+                          "traffic": recorded_traffic(path_name, w.name, plan["partition_tokens"]),
+                          "algorithmic_bytes_per_launch": algo}}
+    if cfg == 4:
+        e = elem(w.dtype)
+        unique = w.unique_blocks * w.block_size * 2 * w.num_kv_heads * w.head_dim * e
+        entry["l2"] = ("the shared prefix and beam prompts are read by several sequences per call and "
+                       "mostly hit L2: logical bytes can exceed the HBM peak")
+        entry["unique_kv_bytes"] = unique
+    else:
+        entry["l2"] = f"inputs larger than L2 (KV {kv / 1e9:.2f} GB > 129 MB): no flush"
+    del g, out, w
+    torch.cuda.empty_cache()
+    return entry
 
 
 def cpu_baseline(w, budget_s):
@@ -471,16 +539,15 @@ def main():
     ms_per_step = total_ms / args.steps
     # The decode call alone (work list + decode kernel, + merge when split), each launch
     # bracketed by events on its stream: the roofline's kernel time.
-    n_k = min(args.steps, 1000)
-    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
-    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
-    for i in range(n_k):
-        k0[i].record(stream)
-        decode(g.q, g.block_tables, g.context_lens)
-        k1[i].record(stream)
+    n_k = max(DECODE_CALLS_MIN, min(args.steps, 1000))
+    decode_ms = decode_call_ms(lambda: decode(g.q, g.block_tables, g.context_lens), stream, n_k)
+    # The other decode workloads the method is measured on, each timed the same way
+    # (only on the default workload, without overrides, so the line stays one run)
+    per_config = None
+    if args.config == 2 and not overrides and not args.identity_tables and args.per_config:
+        per_config = {str(c): measure_config(pkv, c, dev, path, args.partition, n_k) for c in (3, 4, 5)}
     torch.cuda.synchronize()
     clk = clocks.stop()
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k0, k1))
 
     # ---------------- end to end: host inputs in, host output out ----------------
     # The step's inputs sit in one pinned staging buffer (each tensor 256-byte aligned)
@@ -589,6 +656,8 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if per_config is not None:
+        result["per_config"] = per_config
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, args.cpu_seconds)
         cb.pop("_kv_bytes", None)

@@ -39,6 +39,14 @@
  *    call only enqueues work and returns; results are ready when the stream is.
  *    The calls can be captured in a CUDA graph once each kind has run once outside
  *    the capture (the first call sets its kernels' shared-memory limits).
+ *  - Early start: the tensor-core decode's first kernel (its work list) is launched
+ *    as a programmatic dependent of the kernel before it on the stream, so that it
+ *    overlaps paged_kv_append.  Before it waits for that kernel it reads
+ *    context_lens and writes its workspace and the zero rows of out for empty
+ *    sequences.  A kernel that only ends, or one of this library's kernels, is
+ *    always safe before it.  A caller's own kernel that releases its dependents
+ *    early (griddepcontrol.launch_dependents) must do so only after its last write
+ *    to context_lens, and must not touch out or the workspace after that point.
  *  - Alignment: q, k, v, out, k_cache, v_cache must be 16-byte aligned, and
  *    head_dim * element size must be a multiple of 16 bytes.
  *  - Errors: a call returns PKV_OK or an error status and records a message that

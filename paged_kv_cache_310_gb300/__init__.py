@@ -38,7 +38,7 @@ DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_WORKSPACE",
-          4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_INDEX", 6: "PKV_ERR_DEVICE_TIMEOUT"}
+          4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_INDEX", 6: "PKV_ERR_DEVICE_TIMEOUT", 7: "PKV_ERR_OUT_OF_BLOCKS"}
 
 
 class PagedKVError(RuntimeError):
@@ -282,19 +282,22 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
 
 
 def paged_attention_decode_no_alloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, *,
-                                    max_context_len: int | None = None, path: int = PATH_AUTO,
+                                    max_context_len: int, path: int = PATH_AUTO,
                                     partition_tokens: int = 0) -> torch.Tensor:
     """paged_attention_decode without a workspace argument, for callers that cannot
     allocate device memory: the scratch is the library's built-in array of
     ``paged_attention_no_alloc_limit()`` bytes per GPU, shared by every call (calls
-    that overlap on the GPU race on it)."""
+    that overlap on the GPU race on it).
+
+    max_context_len (a host bound on context_lens) is required here: working it out
+    from the device tensor would run a reduction that allocates its result."""
     _need_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
     if q.dim() != 3 or out.shape != q.shape or q.dtype != k_cache.dtype or block_tables.dtype != torch.int32 \
             or context_lens.dtype != torch.int32:
         raise PagedKVError(1, "shape/dtype mismatch between q, out, the caches and the tables")
-    S, Hq, _ = q.shape
     if max_context_len is None:
-        max_context_len = int(context_lens.max()) if S else 0
+        raise PagedKVError(1, "max_context_len is required: computing it on the device would allocate")
+    S, Hq, _ = q.shape
     desc = cache_desc(k_cache)
     cfg = _config(path, partition_tokens)
     _check(library().paged_attention_decode_no_alloc(

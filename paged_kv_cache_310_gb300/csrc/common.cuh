@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pagedkv.h"
 
 namespace pkv {
@@ -117,6 +119,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // an ordinary launch).  grid_dependents_launch() lets the next such kernel start early.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Raises a kernel's dynamic shared-memory limit on the current device.  The attribute
+// belongs to each device, so it is set on the first launch on every device; `done`
+// holds one bit per device index that has it (indices >= 64 set it every time).
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 template <typename Kernel, typename Args>
 cudaError_t launch_dependent(Kernel kernel, int grid, int threads, int smem_bytes, cudaStream_t stream,

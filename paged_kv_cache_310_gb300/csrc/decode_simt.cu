@@ -355,13 +355,9 @@ template <typename T, int D, int GM>
 cudaError_t launch_simt_t(const DecodeParams& p, cudaStream_t stream) {
   using C = Simt<T, D, GM>;
   const size_t smem = C::smem_bytes(p.part_tokens, p.block_size);
-  static bool configured = false;  // raising the limit is idempotent
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<T, D, GM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};  // devices whose limit is raised
+  cudaError_t e = ensure_smem_limit(decode_simt_kernel<T, D, GM>, 200 * 1024, configured);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.max_parts, p.num_kv_heads, p.num_seqs);
   decode_simt_kernel<T, D, GM><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

@@ -761,13 +761,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 template <typename T, int D, int GM>
 cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
   constexpr int smem = TcLayout<D>::kSmemBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, D, GM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};  // devices whose limit is raised
+  cudaError_t e = ensure_smem_limit(decode_tc_kernel<T, D, GM>, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_dependent(decode_tc_kernel<T, D, GM>, grid, TcRoles<GM>::kThreads, smem, stream, args);
 }
 

@@ -658,12 +658,9 @@ bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t toke
 template <typename T, int D>
 cudaError_t launch_prefill_t(const PrefillArgs& args, int grid, cudaStream_t stream) {
   constexpr int smem = PfLayout<D>::kSmemBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};  // devices whose limit is raised
+  cudaError_t e = ensure_smem_limit(prefill_tc_kernel<T, D>, smem, configured);
+  if (e != cudaSuccess) return e;
   prefill_tc_kernel<T, D><<<grid, kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }

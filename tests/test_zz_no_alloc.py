@@ -66,9 +66,36 @@ def test_no_alloc_matches_workspace_entry_point_twice(path):
         got = _no_alloc_via_c_abi(w, g, path, 256)
         torch.cuda.synchronize()
         assert pkv.device_error() == 0
-        err = (got - ref).abs().max().item()
         assert np.isfinite(got.cpu().numpy()).all()
+        err = (got - ref).abs().max().item()
         assert err <= TOL[w.dtype], f"max-abs difference {err:.3g}"
+        # the same kernels with the same plan, only the scratch address differs: the
+        # kernels are deterministic, so the two outputs agree bit for bit
+        assert torch.equal(got, ref), f"outputs differ (max-abs {err:.3g})"
+
+
+def test_python_wrapper_allocates_nothing():
+    """Through the Python binding too, the call takes no device memory from torch's
+    allocator: the counters of allocations do not move over two calls."""
+    w = workloads.random_workload(310_904, num_seqs=6, max_len=2500, min_len=600, num_q_heads=16, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="bf16", canary=False)
+    g = w.to("cuda")
+    out = torch.empty(g.q.shape, dtype=torch.float32, device="cuda")
+    ref = _with_workspace(w, g, pkv.PATH_AUTO, 256)
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_stats()
+    for _ in range(2):
+        pkv.paged_attention_decode_no_alloc(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                                            max_context_len=w.max_context_len, partition_tokens=256)
+    torch.cuda.synchronize()
+    after = torch.cuda.memory_stats()
+    for key in ("allocation.all.allocated", "segment.all.allocated", "allocated_bytes.all.allocated"):
+        assert after.get(key, 0) == before.get(key, 0), f"{key}: {before.get(key, 0)} -> {after.get(key, 0)}"
+    assert pkv.device_error() == 0
+    assert torch.equal(out, ref)
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_attention_decode_no_alloc(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                                            max_context_len=None)
 
 
 def test_no_alloc_rejects_more_than_the_array():
