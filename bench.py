@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--head-dim", type=int, default=0, help="override the workload's head_dim (64/128)")
     ap.add_argument("--num-q-heads", type=int, default=0,
                     help="override the workload's query heads (a multiple of its KV heads: another group size)")
+    ap.add_argument("--dtype", default="", choices=["", "f32", "f16", "bf16"],
+                    help="override the workload's cache dtype")
     ap.add_argument("--identity-tables", action="store_true",
                     help="physical blocks in logical order (contiguous sequences): the indirection A/B")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
@@ -60,6 +62,7 @@ def parse():
 
 
 KERNEL_SOURCES = {"tensor_core": ["common.cuh", "decode_tc.cu", "launch.h", "tc_util.cuh", "tcgen05.cuh"],
+                  "tensor_core_f32": ["common.cuh", "decode_tc32.cu", "launch.h", "tc_util.cuh", "tcgen05.cuh"],
                   "cuda_core": ["common.cuh", "decode_simt.cu", "launch.h"],
                   "prefill": ["common.cuh", "prefill_tc.cu", "launch.h", "tc_util.cuh", "tcgen05.cuh"]}
 
@@ -178,6 +181,13 @@ def decode_call_ms(call, stream, n):
     return statistics.mean(a.elapsed_time(b) for a, b in zip(k0, k1))
 
 
+def traffic_path(plan_path, dtype):
+    """Key of the kernel sources a decode plan runs (profiles/traffic.json)."""
+    if plan_path == 2:
+        return "tensor_core_f32" if dtype == torch.float32 else "tensor_core"
+    return "cuda_core"
+
+
 def measure_config(pkv, cfg, dev, path, partition, n_calls):
     """Decode-call roofline of workload `cfg` (its step's copies and append done once
     first, as the step does), inputs resident in HBM."""
@@ -206,6 +216,7 @@ def measure_config(pkv, cfg, dev, path, partition, n_calls):
     plan = pkv.paged_attention_plan(S, Hq, maxL, g.k_cache, path=path, partition_tokens=partition)
     path_name = {1: "cuda_core", 2: "tensor_core"}[plan["path"]]
     kv, algo = roofline_bytes(w, elem(out.dtype))
+    sources = traffic_path(plan["path"], w.dtype)
     peak, peak_kind = peaks()
     achieved = algo / (ms * 1e-3) / 1e9
     entry = {"workload": w.name, "path": path_name, "partition_tokens": plan["partition_tokens"],
@@ -213,7 +224,7 @@ def measure_config(pkv, cfg, dev, path, partition, n_calls):
              "kv_gbs": kv / (ms * 1e-3) / 1e9, "seq_tokens_per_s": int(w.context_lens.sum()) / (ms * 1e-3),
              "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                           "frac": achieved / peak, "peak_source": peak_kind,
-                          "traffic": recorded_traffic(path_name, w.name, plan["partition_tokens"]),
+                          "traffic": recorded_traffic(sources, w.name, plan["partition_tokens"]),
                           "algorithmic_bytes_per_launch": algo}}
     if cfg == 4:
         e = elem(w.dtype)
@@ -483,7 +494,7 @@ def main():
     path = {"auto": pkv.PATH_AUTO, "cuda_core": pkv.PATH_CUDA_CORE, "tensor_core": pkv.PATH_TENSOR_CORE}[args.path]
     # every rank decodes its own batch of the same workload shape (independent replicas)
     overrides = {k: v for k, v in (("block_size", args.block_size), ("head_dim", args.head_dim),
-                                   ("num_q_heads", args.num_q_heads)) if v}
+                                   ("num_q_heads", args.num_q_heads), ("dtype", args.dtype)) if v}
     w = workloads.make_workload(args.config, canary=False, pool_device=dev, shuffle=not args.identity_tables,
                                 **overrides)
     g = w.to(dev)
@@ -493,21 +504,30 @@ def main():
     host_pairs = w.cow_pairs.cpu()
     stream = torch.cuda.current_stream(dev)
 
-    def decode(q, tables, lens, o=out):
-        pkv.paged_attention_decode(q, g.k_cache, g.v_cache, tables, lens, w.scale, o, max_context_len=maxL,
-                                   path=path, partition_tokens=args.partition)
-
-    def step(q, kn, vn, slots, tables, lens, o=out):
+    # A step is the library's three calls, each prepared once (arguments checked and
+    # marshalled) and then replayed on the stream, as a serving loop over fixed buffers
+    # would: copy-on-write copies, the append, decode.
+    def step_calls(q, kn, vn, slots, tables, lens, o):
+        calls = []
         if g.cow_pairs.numel():
-            pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache)
-        pkv.paged_kv_append(kn, vn, slots, g.k_cache, g.v_cache)
-        decode(q, tables, lens, o)
+            calls.append(pkv.prepare_block_copy(g.cow_pairs, g.k_cache, g.v_cache))
+        calls.append(pkv.prepare_kv_append(kn, vn, slots, g.k_cache, g.v_cache))
+        calls.append(pkv.prepare_attention_decode(q, g.k_cache, g.v_cache, tables, lens, w.scale, o,
+                                                  max_context_len=maxL, path=path,
+                                                  partition_tokens=args.partition))
+        return calls
 
-    args_dev = (g.q, g.k_new, g.v_new, g.slot_mapping, g.block_tables, g.context_lens)
+    handle = stream.cuda_stream
+    resident = step_calls(g.q, g.k_new, g.v_new, g.slot_mapping, g.block_tables, g.context_lens, out)
+
+    def step(calls=resident):
+        for call in calls:
+            call(handle)
+
     if g.cow_pairs.numel():  # validate the pairs once on the host
         pkv.paged_block_copy(g.cow_pairs, g.k_cache, g.v_cache, host_pairs=host_pairs)
     for _ in range(max(3, args.warmup)):
-        step(*args_dev)
+        step()
     torch.cuda.synchronize()
     if pkv.device_error() != 0:
         raise SystemExit("device error flag set during warm-up")
@@ -527,7 +547,7 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_begin.record(stream)
     for _ in range(args.steps):
-        step(*args_dev)
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -540,7 +560,7 @@ def main():
     # The decode call alone (work list + decode kernel, + merge when split), each launch
     # bracketed by events on its stream: the roofline's kernel time.
     n_k = max(DECODE_CALLS_MIN, min(args.steps, 1000))
-    decode_ms = decode_call_ms(lambda: decode(g.q, g.block_tables, g.context_lens), stream, n_k)
+    decode_ms = decode_call_ms(lambda: resident[-1](handle), stream, n_k)
     # The other decode workloads the method is measured on, each timed the same way
     # (only on the default workload, without overrides, so the line stays one run)
     per_config = None
@@ -574,12 +594,14 @@ def main():
     d2h = out_host[0].numel() * out_host[0].element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n_e2e = max(3, args.e2e_steps)
+    e2e_calls = [step_calls(*dev_in[b], outs[b]) for b in range(2)]
+    # per buffer b: its inputs are on the device / its kernels are done with it / its
+    # output is back on the host (events re-recorded each step)
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    fetched = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_run(n):
-        ev = lambda: torch.cuda.Event()  # noqa: E731
-        uploaded = [None, None]   # step's inputs are on the device
-        consumed = [None, None]   # step's kernels are done with staging / output buffer b
-        fetched = [None, None]    # output buffer b is back on the host
         e0 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         up.wait_event(e0)
@@ -587,10 +609,9 @@ def main():
         def upload(i):
             b = i % 2
             with torch.cuda.stream(up):
-                if consumed[b] is not None:
+                if i >= 2:
                     up.wait_event(consumed[b])
                 stage_dev[b].copy_(stage_host, non_blocking=True)
-                uploaded[b] = ev()
                 uploaded[b].record(up)
 
         upload(0)
@@ -599,19 +620,16 @@ def main():
             if i + 1 < n:
                 upload(i + 1)
             stream.wait_event(uploaded[b])
-            if fetched[b] is not None:
+            if i >= 2:
                 stream.wait_event(fetched[b])
-            step(*dev_in[b], o=outs[b])
-            consumed[b] = ev()
+            step(e2e_calls[b])
             consumed[b].record(stream)
             with torch.cuda.stream(down):
                 down.wait_event(consumed[b])
                 out_host[b].copy_(outs[b], non_blocking=True)
-                fetched[b] = ev()
                 fetched[b].record(down)
-        for f in fetched:
-            if f is not None:
-                stream.wait_event(f)
+        for i in range(max(0, n - 2), n):
+            stream.wait_event(fetched[i % 2])
         e1 = torch.cuda.Event(enable_timing=True)
         e1.record(stream)
         return e0, e1
@@ -647,9 +665,13 @@ def main():
         "hbm_frac_step": (algo_bytes / (ms_per_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": recorded_traffic({1: "cuda_core", 2: "tensor_core"}[plan["path"]], w.name,
+                     "traffic": recorded_traffic(traffic_path(plan["path"], w.dtype), w.name,
                                                  plan["partition_tokens"]),
-                     "kernel": "paged_attention_decode (work list + decode_tc, or decode_simt + merge)",
+                     "kernel": {"tensor_core": "paged_attention_decode (work list + decode_tc, + merge when split)",
+                                "tensor_core_f32": "paged_attention_decode (work list + decode_tc32, + merge when "
+                                                   "split)",
+                                "cuda_core": "paged_attention_decode (decode_simt, + merge when split)"}[
+                         traffic_path(plan["path"], w.dtype)],
                      "algorithmic_bytes_per_launch": algo_bytes, "ms_per_launch": decode_ms},
         "e2e": {"value": whole_job_rate(world, kv_bytes, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -372,6 +372,18 @@ pkv_status paged_kv_device_error(void* stream);
  */
 pkv_status paged_kv_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
+/*
+ * Diagnostic (no counterpart on the pages): set the bound of the pipeline waits in
+ * the decode and prefill kernels launched from now on, process-wide (0 restores the
+ * default of 2 s; at most 5 s, else PKV_ERR_INVALID_ARG).  A bound far below a
+ * healthy wait (say 1 us) makes a normal call give up part-way: its kernels then take
+ * their abort path -- they wait (each up to 2 s) for the copies and MMAs they have in
+ * flight, free their tensor memory, record PKV_ERR_DEVICE_TIMEOUT in the device flag
+ * and return -- so that path can be exercised without any real fault.  The output of
+ * such a call is undefined.  Not for production use.
+ */
+pkv_status paged_kv_set_wait_limit(uint64_t limit_ns);
+
 /* Library version, e.g. "0.1.0". */
 const char* paged_kv_version(void);
 

@@ -27,6 +27,7 @@ __all__ = [
     "paged_attention_workspace_bytes", "paged_attention_decode_no_alloc", "paged_attention_no_alloc_limit",
     "paged_kv_gather", "paged_block_swap_out", "paged_block_swap_in", "paged_attention_prefill", "device_error", "declared_functions",
     "PATH_AUTO", "PATH_CUDA_CORE", "PATH_TENSOR_CORE",
+    "PreparedCall", "prepare_kv_append", "prepare_block_copy", "prepare_attention_decode", "set_wait_limit",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -103,6 +104,7 @@ def library():
             "paged_attention_no_alloc_limit": [],
             "paged_kv_device_error": [vp],
             "paged_kv_selftest_wait_timeout": [ctypes.c_uint64, vp],
+            "paged_kv_set_wait_limit": [ctypes.c_uint64],
             "paged_kv_last_error": [],
             "paged_kv_version": [],
         }
@@ -148,8 +150,36 @@ def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
     return CacheDesc(nb, bs, hkv, d, DTYPE_CODE[k_cache.dtype])
 
 
-def paged_kv_append(k, v, slot_mapping, k_cache, v_cache) -> None:
-    """k, v [T, Hkv, D] -> k_cache/v_cache rows given by slot_mapping (int64 [T])."""
+class PreparedCall:
+    """One library call whose arguments were checked and marshalled once.
+
+    Calling it enqueues the same work again on `stream` (a torch.cuda.Stream or a raw
+    cudaStream_t handle; default: the device's current stream), with none of the
+    per-call argument checks and ctypes conversions of the plain functions -- what a
+    serving loop that replays the same buffers every step wants.  The tensors it was
+    made from stay referenced by it; their contents may change between calls, their
+    storage must not (no reallocation, resize or reshaping in place)."""
+
+    __slots__ = ("_fn", "_args", "_device", "_keep")
+
+    def __init__(self, fn, args, device, keep):
+        self._fn, self._args, self._device, self._keep = fn, tuple(args), device, keep
+
+    def __call__(self, stream=None) -> None:
+        if stream is None:
+            handle = torch.cuda.current_stream(self._device).cuda_stream
+        else:
+            handle = stream if isinstance(stream, int) else stream.cuda_stream
+        status = self._fn(*self._args, ctypes.c_void_p(handle))
+        if status != 0:
+            raise PagedKVError(status, library().paged_kv_last_error().decode())
+
+
+def _run(prepared: PreparedCall) -> None:
+    prepared()
+
+
+def _append_call(k, v, slot_mapping, k_cache, v_cache) -> PreparedCall:
     _need_cuda(k, v, slot_mapping, k_cache, v_cache)
     if slot_mapping.dtype != torch.int64 or k.dtype != k_cache.dtype or v.dtype != k_cache.dtype:
         raise PagedKVError(1, "slot_mapping must be int64 and k/v must have the cache dtype")
@@ -157,15 +187,22 @@ def paged_kv_append(k, v, slot_mapping, k_cache, v_cache) -> None:
             or tuple(k.shape[1:]) != (k_cache.shape[1], k_cache.shape[3]) or k_cache.shape != v_cache.shape:
         raise PagedKVError(1, "shape mismatch between k, v, slot_mapping and the caches")
     desc = cache_desc(k_cache)
-    _check(library().paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.numel(),
-                                     _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _stream(k_cache)))
+    args = (_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache),
+            ctypes.byref(desc))
+    return PreparedCall(library().paged_kv_append, args, k_cache.device, (k, v, slot_mapping, k_cache, v_cache, desc))
 
 
-def paged_block_copy(src_dst_pairs, k_cache, v_cache, host_pairs: torch.Tensor | None = None) -> None:
-    """Copy block src to block dst for each row of src_dst_pairs (device int64 [n, 2]).
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache) -> None:
+    """k, v [T, Hkv, D] -> k_cache/v_cache rows given by slot_mapping (int64 [T])."""
+    _run(_append_call(k, v, slot_mapping, k_cache, v_cache))
 
-    host_pairs (CPU int64 [n, 2], optional) lets the library validate the pairs.
-    """
+
+def prepare_kv_append(k, v, slot_mapping, k_cache, v_cache) -> PreparedCall:
+    """paged_kv_append with its arguments bound once (see PreparedCall)."""
+    return _append_call(k, v, slot_mapping, k_cache, v_cache)
+
+
+def _block_copy_call(src_dst_pairs, k_cache, v_cache, host_pairs) -> PreparedCall:
     _need_cuda(src_dst_pairs, k_cache, v_cache)
     if src_dst_pairs.dtype != torch.int64 or (src_dst_pairs.numel() % 2):
         raise PagedKVError(1, "src_dst_pairs must be int64 [n, 2]")
@@ -175,8 +212,23 @@ def paged_block_copy(src_dst_pairs, k_cache, v_cache, host_pairs: torch.Tensor |
             raise PagedKVError(1, "host_pairs must be a CPU copy of src_dst_pairs")
     desc = cache_desc(k_cache)
     n = src_dst_pairs.numel() // 2
-    _check(library().paged_block_copy(_ptr(src_dst_pairs), _ptr(host_pairs), n, _ptr(k_cache),
-                                      _ptr(v_cache), ctypes.byref(desc), _stream(k_cache)))
+    args = (_ptr(src_dst_pairs), _ptr(host_pairs), n, _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc))
+    return PreparedCall(library().paged_block_copy, args, k_cache.device,
+                        (src_dst_pairs, host_pairs, k_cache, v_cache, desc))
+
+
+def paged_block_copy(src_dst_pairs, k_cache, v_cache, host_pairs: torch.Tensor | None = None) -> None:
+    """Copy block src to block dst for each row of src_dst_pairs (device int64 [n, 2]).
+
+    host_pairs (CPU int64 [n, 2], optional) lets the library validate the pairs.
+    """
+    _run(_block_copy_call(src_dst_pairs, k_cache, v_cache, host_pairs))
+
+
+def prepare_block_copy(src_dst_pairs, k_cache, v_cache, host_pairs: torch.Tensor | None = None) -> PreparedCall:
+    """paged_block_copy with its arguments bound once (see PreparedCall); the pairs are
+    validated against host_pairs, when given, at every call."""
+    return _block_copy_call(src_dst_pairs, k_cache, v_cache, host_pairs)
 
 
 def _swap_buffers(ids, k_cache, host_k, host_v):
@@ -253,6 +305,24 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     max_context_len: host upper bound on context_lens (computed with a device sync
     when omitted).  workspace: uint8 device buffer, allocated and cached when omitted.
     """
+    _run(_decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len,
+                      workspace, path, partition_tokens))
+    return out
+
+
+def prepare_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, *,
+                             max_context_len: int, workspace: torch.Tensor | None = None,
+                             path: int = PATH_AUTO, partition_tokens: int = 0) -> PreparedCall:
+    """paged_attention_decode with its arguments bound once (see PreparedCall).
+    max_context_len stays the bound of every later call."""
+    if max_context_len is None:
+        raise PagedKVError(1, "max_context_len is required for a prepared decode")
+    return _decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len, workspace,
+                        path, partition_tokens)
+
+
+def _decode_call(q, k_cache, v_cache, block_tables, context_lens, scale, out, max_context_len, workspace, path,
+                 partition_tokens) -> PreparedCall:
     _need_cuda(q, k_cache, v_cache, block_tables, context_lens, out, workspace)
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise PagedKVError(1, "block_tables and context_lens must be int32")
@@ -274,11 +344,11 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     if workspace is None:
         workspace = _workspace(q.device, need)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.paged_attention_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                      block_tables.shape[1], _ptr(context_lens), S, Hq, max_context_len,
-                                      float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
-                                      ws_bytes, ctypes.byref(desc), ctypes.byref(cfg), _stream(q)))
-    return out
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            S, Hq, max_context_len, ctypes.c_float(float(scale)), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
+            ws_bytes, ctypes.byref(desc), ctypes.byref(cfg))
+    return PreparedCall(lib.paged_attention_decode, args, q.device,
+                        (q, k_cache, v_cache, block_tables, context_lens, out, workspace, desc, cfg))
 
 
 def paged_attention_decode_no_alloc(q, k_cache, v_cache, block_tables, context_lens, scale, out, *,
@@ -367,6 +437,12 @@ def selftest_wait_timeout(limit_ns: int = 50_000_000) -> None:
     """Run the bounded-wait self-test kernel on the current stream (see the header)."""
     stream = torch.cuda.current_stream()
     _check(library().paged_kv_selftest_wait_timeout(int(limit_ns), ctypes.c_void_p(stream.cuda_stream)))
+
+
+def set_wait_limit(limit_ns: int = 0) -> None:
+    """Bound of the decode and prefill kernels' pipeline waits for later launches
+    (0 = the default 2 s).  A tiny bound forces their abort path; see the header."""
+    _check(library().paged_kv_set_wait_limit(int(limit_ns)))
 
 
 def device_error(device=None) -> int:

@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points of libpagedkv.so (declared in
 // include/pagedkv.h): argument checks, launch configuration, the device error flag.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -31,6 +32,10 @@ pkv_status fail(pkv_status st, const char* fmt, ...) {
 pkv_status cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+// Bound of the decode and prefill kernels' pipeline waits (kWaitLimitNs unless a test
+// lowers it with paged_kv_set_wait_limit); read once per launch.
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_flag_mutex;
@@ -97,13 +102,16 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   if (path < PKV_PATH_AUTO || path > PKV_PATH_TENSOR_CORE)
     return fail(PKV_ERR_INVALID_ARG, "decode path %d", path);
   const bool tc_ok = tc_supported(c->dtype, c->head_dim, group, c->block_size);
-  // Tensor cores wherever they apply: at G >= 2 QK and PV are real contractions, and at
-  // G = 1 the persistent TMA/tcgen05 kernel still streams K/V slightly faster (0.977 vs
-  // 0.922 of copy bandwidth on a 64 x 32-head bf16 batch).  f32 uses CUDA cores.
-  if (path == PKV_PATH_AUTO) path = tc_ok ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
+  // Tensor cores wherever they apply to 16-bit caches: at G >= 2 QK and PV are real
+  // contractions, and at G = 1 the persistent TMA/tcgen05 kernel still streams K/V
+  // slightly faster (0.977 vs 0.922 of copy bandwidth on a 64 x 32-head bf16 batch).
+  // f32 caches take the tf32 kernel from 4 query heads per KV head; below that the
+  // CUDA-core kernel streams at copy bandwidth with no extra conversion work.
+  if (path == PKV_PATH_AUTO)
+    path = tc_ok && (c->dtype != PKV_F32 || group >= 4) ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
   if (path == PKV_PATH_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED,
-                "tensor-core path needs f16/bf16, head_dim 64 or 128, group <= 16 (group %d)", group);
+                "tensor-core path needs head_dim 64 or 128 and group <= 16 (<= 8 for f32) (group %d)", group);
   if (path == PKV_PATH_CUDA_CORE && group > 8)
     return fail(PKV_ERR_UNSUPPORTED, "CUDA-core path supports query-head groups <= 8 (group %d)", group);
   if (static_cast<int64_t>(c->num_blocks) * c->num_kv_heads * c->block_size > (int64_t{1} << 30))
@@ -187,6 +195,13 @@ pkv_status paged_kv_device_error(void* stream) {
   }
   if (value & kErrTimeout) return fail(PKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (flag 0x%x)", value);
   if (value) return fail(PKV_ERR_DEVICE_INDEX, "a kernel met an out-of-range index or length (flag 0x%x)", value);
+  return PKV_OK;
+}
+
+pkv_status paged_kv_set_wait_limit(uint64_t limit_ns) {
+  if (limit_ns > 5000000000ull)
+    return fail(PKV_ERR_INVALID_ARG, "limit_ns %llu above 5 s", (unsigned long long)limit_ns);
+  g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns);
   return PKV_OK;
 }
 
@@ -398,6 +413,7 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   p.max_parts = plan.max_parts;
   p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
+  p.wait_limit_ns = g_wait_limit_ns.load();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = plan.path == PKV_PATH_TENSOR_CORE ? launch_decode_tc(p, cache->dtype, s)
@@ -430,7 +446,7 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d", num_q_heads,
                 cache->num_kv_heads);
   const int group = num_q_heads / cache->num_kv_heads;
-  if (!tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
+  if (cache->dtype == PKV_F32 || !tc_supported(cache->dtype, cache->head_dim, group, cache->block_size))
     return fail(PKV_ERR_UNSUPPORTED, "prefill needs f16/bf16, head_dim 64 or 128 and query-head groups <= 16");
   if (cache->num_kv_heads > 4095)  // a work-list entry packs the KV head into 12 bits
     return fail(PKV_ERR_UNSUPPORTED, "prefill supports at most 4095 KV heads (%d)", cache->num_kv_heads);
@@ -478,6 +494,7 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
   p.head_dim = cache->head_dim;
   p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = launch_prefill_tc(p, cache->dtype, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : cuda_fail(e, "prefill launch");
 }

@@ -196,10 +196,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Below this limit a wait polls with the non-blocking probe and reads the clock every
+// round: mbarrier.try_wait may suspend the thread for longer than such a limit, so a
+// wait could otherwise never notice that it ran out.
+constexpr uint64_t kPollBelowNs = 1000000ull;
+
 // Wait for the phase of `bar` with the given parity to complete; false if the wait
 // ran past limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
+  if (limit_ns < kPollBelowNs) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_test_wait(bar, parity))
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {

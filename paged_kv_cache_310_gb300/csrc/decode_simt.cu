@@ -151,7 +151,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
       int issued = 0;
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % C::kStages;
-        if (c >= C::kStages && !mbar_wait(&empty[st], ((c / C::kStages) - 1) & 1)) {
+        if (c >= C::kStages && !mbar_wait(&empty[st], ((c / C::kStages) - 1) & 1, p.wait_limit_ns)) {
           set_error(p.err, kErrTimeout);
           atomicMin(&flags[0], c);
           break;
@@ -198,7 +198,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     for (int c = 0; c < nchunks; ++c) {
       const int st = c % C::kStages;
       // warp-uniform: every lane must take the same branch before the shuffles below
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / C::kStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / C::kStages) & 1, p.wait_limit_ns))) {
         if (lane == 0) {
           set_error(p.err, kErrTimeout);
           atomicMin(&flags[0], c);

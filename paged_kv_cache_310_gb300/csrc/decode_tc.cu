@@ -76,9 +76,13 @@ constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (u
 // 4 query heads per KV head warps 7-10 softmax too: a warp reads the TMEM lane
 // quarter of its index mod 4, so two warps share each quarter (each 32 tokens) and
 // take half of the heads each, which halves the softmax work per thread.
+#ifndef PKV_TC_SPLIT_G16
+#define PKV_TC_SPLIT_G16 4
+#endif
 template <int GM>
 struct TcRoles {
-  static constexpr int kSplit = GM >= 4 ? 2 : 1;      // softmax warps per lane quarter
+  // softmax warps per lane quarter
+  static constexpr int kSplit = GM >= 16 ? PKV_TC_SPLIT_G16 : GM >= 4 ? 2 : 1;
   static constexpr int kHeads = GM / kSplit;          // query heads per softmax thread
   static constexpr int kSoftmaxThreads = 128 * kSplit;
   static constexpr int kThreads = kSoftmaxThreads + 96;
@@ -191,6 +195,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int* kissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 8);   // K chunks issued
   int* vissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 12);  // V chunks issued
+  int* qissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 16);  // query tiles issued
   const int G = p.group;
 
   if (threadIdx.x == 0) {
@@ -214,6 +219,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     *abort_flag = 0;
     *kissued_slot = 0;
     *vissued_slot = 0;
+    *qissued_slot = 0;
     fence_barrier_init();
   }
   if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       const Item it = unpack_item(cur.cur, p.part_tokens);
       const int qb = j & 1;
       if (lane == 0) {
-        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err);
+        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
         if (ok) {
           mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
           unsigned char* qdst = smem + kOffQ + qb * kQBytes;
@@ -259,6 +265,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
 #pragma unroll
           for (int cb = 0; cb < L::kBlocks; ++cb)
             tma_load_2d(qdst + cb * kQHalfBytes, &a.tq, 64 * cb, qrow, &bars.qfull[qb], pol_keep);
+          *qissued_slot = j + 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
-          ok = c < kKStages || wait_role(&bars.kempty[st], ((c / kKStages) - 1) & 1, abort_flag, p.err);
+          ok = c < kKStages || wait_role(&bars.kempty[st], ((c / kKStages) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
           if (ok) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         const bool live = lane < blocks_per_chunk && lb * bs < it.t0 + it.ntok;
         int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
         if (lane == 0) {
-          ok = c < kVStages || wait_role(&bars.vempty[st], ((c / kVStages) - 1) & 1, abort_flag, p.err);
+          ok = c < kVStages || wait_role(&bars.vempty[st], ((c / kVStages) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
           if (ok) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -416,7 +423,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         idle_since = global_timer_ns();
       } else {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-        if (__any_sync(0xffffffffu, global_timer_ns() - idle_since > kWaitLimitNs)) {
+        if (__any_sync(0xffffffffu, global_timer_ns() - idle_since > p.wait_limit_ns)) {
           if (lane == 0) {
             *abort_flag = 1;
             set_error(p.err, kErrTimeout);
@@ -431,7 +438,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     constexpr int HG = R::kHeads;              // heads of this thread: h0 .. h0 + HG - 1
     constexpr int NS = R::kSoftmaxThreads;     // threads in the softmax barriers
     const int quarter = warp & 3;              // TMEM lane quarter this warp may read
-    const int h0 = warp >= 7 ? HG : 0;         // first head (the second warp of a quarter: the upper half)
+    // first head: warps 0-3 take the lowest HG heads of their quarter, each further set
+    // of four warps (7-10, 11-14, ...) the next HG
+    const int h0 = warp < 4 ? 0 : ((warp - 7) / 4 + 1) * HG;
     const int t = quarter * 32 + lane;         // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float m[HG], lp[HG], alpha[HG], alpha_pend[HG], acc[HG];
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     // the caller then stops at the next collective barrier.
     auto consume = [&](int cp) -> bool {
       const int pb = cp & 1;
-      if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err)))
+      if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)))
         return false;
       tc_fence_after();
       // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16
@@ -463,6 +472,8 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           o[h] = (h0 & 2) ? a4[(2 + h) & 3] : a4[h];
           olo[h] = (h0 & 2) ? b4[(2 + h) & 3] : b4[h];
         }
+      } else if (HG == 4) {
+        tmem_load4x2(ob, ob + 16, o, olo);
       } else {
         tmem_load8x2(ob, ob + 16, o, olo);
       }
@@ -512,7 +523,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       }
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
-        const bool wok = __all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err));
+        const bool wok = __all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err, p.wait_limit_ns));
         float sv[HG];
         if (wok) {
           tc_fence_after();
@@ -602,6 +613,10 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         } else if (GM == 8) {  // each of the two warps writes its four heads' half of a group
           *reinterpret_cast<uint2*>(pdst + h0 * 2) = make_uint2(hw[0], hw[1]);
           *reinterpret_cast<uint2*>(pdst + kChunk * 16 + h0 * 2) = make_uint2(lw[0], lw[1]);
+        } else if (HG == 4) {  // 16 heads over four warps: each writes half of a column group
+          const int gh = h0 / 8, off = (h0 & 7) * 2;
+          *reinterpret_cast<uint2*>(pdst + gh * kChunk * 16 + off) = make_uint2(hw[0], hw[1]);
+          *reinterpret_cast<uint2*>(pdst + (2 + gh) * kChunk * 16 + off) = make_uint2(lw[0], lw[1]);
         } else {
           const int gh = h0 / 8;  // this warp's column group of hi parts
           *reinterpret_cast<uint4*>(pdst + gh * kChunk * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -615,7 +630,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           // (warp-uniform) the chunk's V must have landed before its tail rows are zeroed
           const bool v_ok = rows_valid >= rows_loaded ||
                             __all_sync(0xffffffffu, wait_role(&bars.vfull[c % kVStages], (c / kVStages) & 1,
-                                                              abort_flag, p.err));
+                                                              abort_flag, p.err, p.wait_limit_ns));
           if (v_ok && t >= rows_valid && t < rows_loaded) {
             unsigned char* vrow = smem + kOffV + (c % kVStages) * kTileBytes + (t >> 3) * kGroupBytes + (t & 7) * 128;
 #pragma unroll
@@ -665,16 +680,26 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     if (warp == 4 && lane == 0) {
       for (int c = max(0, *kissued_slot - kKStages); c < *kissued_slot; ++c)
         if (!mbar_wait(&bars.kfull[c % kKStages], (c / kKStages) & 1)) break;
+      // the query tiles of the last two items (each has its own buffer and barrier)
+      for (int jj = max(0, *qissued_slot - 2); jj < *qissued_slot; ++jj)
+        if (!mbar_wait(&bars.qfull[jj & 1], (jj >> 1) & 1)) break;
     }
     if (warp == 6 && lane == 0) {
       for (int c = max(0, *vissued_slot - kVStages); c < *vissued_slot; ++c)
         if (!mbar_wait(&bars.vfull[c % kVStages], (c / kVStages) & 1)) break;
     }
-    if (warp == 5 && lane == 0) {
-      mbar_init(bars.drain, 1);
-      fence_barrier_init();
+    if (warp == 5) {
+      // every lane commits (the MMAs went out from whichever lane was elected; a lane
+      // that issued none arrives at once), so the barrier completes only when all of
+      // the warp's MMAs have
+      if (lane == 0) {
+        mbar_init(bars.drain, 32);
+        fence_barrier_init();
+      }
+      __syncwarp();
       mma_commit(bars.drain);
       mbar_wait(bars.drain, 0);
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -745,7 +770,8 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
 }
 
 // 2-D map over rows of head_dim 16-bit elements, box 64 x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16, int head_dim) {
+bool make_map_uncached(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16,
+                       int head_dim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
@@ -756,6 +782,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool bf16, int head_dim) {
+  return cached_map(m, MapKey{base, rows, box_rows, 2, bf16 ? 2 : 1, head_dim}, [&](CUtensorMap* out) {
+    return make_map_uncached(out, base, rows, box_rows, bf16, head_dim);
+  });
 }
 
 template <typename T, int D, int GM>
@@ -785,12 +817,22 @@ cudaError_t launch_tc_d(const TcArgs& args, int grid, cudaStream_t stream) {
 }  // namespace
 
 bool tc_supported(int dtype, int head_dim, int group, int block_size) {
-  return (dtype == PKV_F16 || dtype == PKV_BF16) && (head_dim == 64 || head_dim == 128) && group >= 1 &&
-         group <= kN &&
+  const int max_group = dtype == PKV_F32 ? 8 : kN;  // f32: the tf32 kernel's N holds 8 heads twice
+  return (dtype == PKV_F16 || dtype == PKV_BF16 || dtype == PKV_F32) && (head_dim == 64 || head_dim == 128) &&
+         group >= 1 && group <= max_group &&
          (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream) {
+  if (dtype == PKV_F32) {  // the tf32 kernel (decode_tc32.cu) over the same work list
+    const int items = p.max_parts * p.num_seqs * p.num_kv_heads;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int grid = items < sms ? items : sms;
+    cudaError_t e = launch_dependent(work_list_kernel<float>, 1, kListThreads, 0, stream, p);
+    if (e != cudaSuccess || grid == 0) return e;
+    return launch_decode_tc32(p, grid, stream);
+  }
   TcArgs args;
   args.p = p;
   const bool bf16 = dtype == PKV_BF16;

@@ -28,6 +28,7 @@ struct DecodeParams {
   int32_t part_tokens, max_parts;
   int32_t out_f32;   // 1: out is fp32, 0: out has the cache dtype
   float scale_log2;  // softmax scale * log2(e): scores live in the exp2 domain
+  uint64_t wait_limit_ns;  // bound of every pipeline wait (kWaitLimitNs unless a test lowers it)
 };
 
 // Multi-token causal (prefill) attention, tensor cores; f16/bf16, head_dim 64 or 128.
@@ -47,6 +48,7 @@ struct PrefillParams {
   int32_t head_dim;  // 64 or 128
   int32_t out_f32;
   float scale_log2;
+  uint64_t wait_limit_ns;  // bound of every pipeline wait (kWaitLimitNs unless a test lowers it)
 };
 int prefill_tile_tokens(int group);
 size_t prefill_max_items(int num_seqs, int num_query_tokens, int num_kv_heads, int group);
@@ -59,6 +61,9 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t st
 constexpr int kTcMaxPartition = 4096;
 bool tc_supported(int dtype, int head_dim, int group, int block_size);
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream);
+// The f32 (tf32, split-operand) decode kernel over a work list already launched on the
+// stream; head_dim 64/128, group <= 8.
+cudaError_t launch_decode_tc32(const DecodeParams& p, int grid, cudaStream_t stream);
 // Partition merge for sequences longer than one partition.
 cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream);
 

@@ -176,7 +176,7 @@ __device__ __forceinline__ bool load_chunks(const PrefillParams& p, const Item& 
     int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
     bool ok = true;
     if (lane == 0) {
-      ok = c < kStages || wait_role(&empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err);
+      ok = c < kStages || wait_role(&empty[st], ((c / kStages) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
       if (ok) mbar_arrive_expect_tx(&full[st], kKVTile);
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // ---- both tiles' queries into buffer j & 1 (free once item j - 2's QKs completed) ----
       const int qb = j & 1;
       if (lane == 0) {
-        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err);
+        ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
         if (ok) mbar_arrive_expect_tx(&bars.qfull[qb], kQItem);
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroup, kLayoutSwizzle128);
     const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), 1024, kGroup, kLayoutSwizzle128);
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, wait_role(bar, parity, abort_flag, p.err));
+      return __all_sync(0xffffffffu, wait_role(bar, parity, abort_flag, p.err, p.wait_limit_ns));
     };
     // QK side: next chunk qc (global), its stage / phase, its place in the item
     ItemCursor qcur;
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
     // Warp-uniform: has this tile's PV of chunk cc completed?
     auto pv_done = [&](int cc) -> bool {
-      return __all_sync(0xffffffffu, wait_role(bars.pvdone(grp, cc & 1), (cc >> 1) & 1, abort_flag, p.err));
+      return __all_sync(0xffffffffu, wait_role(bars.pvdone(grp, cc & 1), (cc >> 1) & 1, abort_flag, p.err, p.wait_limit_ns));
     };
     // A finished item's output rows: O / l (O is final: its last PV was waited for).
     auto finish = [&](int row, float lsum) {
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
         const uint32_t sbuf = lane_base + sb * 64;
-        if (!__all_sync(0xffffffffu, wait_role(bars.sfull(grp, sb), (c >> 1) & 1, abort_flag, p.err))) {
+        if (!__all_sync(0xffffffffu, wait_role(bars.sfull(grp, sb), (c >> 1) & 1, abort_flag, p.err, p.wait_limit_ns))) {
           ok = false;
           break;
         }
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // there would survive a zero weight).  Both groups write the same zeros.
         const int rows_needed = it.last + 1 - kbase;
         if (rows_needed < kKC) {  // warp-uniform; V of this chunk must have landed first
-          if (!__all_sync(0xffffffffu, wait_role(&bars.vfull[c % kStages], (c / kStages) & 1, abort_flag, p.err))) {
+          if (!__all_sync(0xffffffffu, wait_role(&bars.vfull[c % kStages], (c / kStages) & 1, abort_flag, p.err, p.wait_limit_ns))) {
             ok = false;
             break;
           }
@@ -585,11 +585,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int c = max(0, *vissued_slot - kStages); c < *vissued_slot; ++c)
         if (!mbar_wait(&bars.vfull[c % kStages], (c / kStages) & 1)) break;
     }
-    if (warp == kMmaWarp && lane == 0) {
-      mbar_init(bars.drain, 1);
-      fence_barrier_init();
+    if (warp == kMmaWarp) {
+      // every lane commits (the MMAs went out from whichever lane was elected; a lane
+      // that issued none arrives at once), so the barrier completes only when all of
+      // the warp's MMAs have
+      if (lane == 0) {
+        mbar_init(bars.drain, 32);
+        fence_barrier_init();
+      }
+      __syncwarp();
       mma_commit(bars.drain);
       mbar_wait(bars.drain, 0);
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -642,7 +649,8 @@ __global__ void __launch_bounds__(kListThreads) prefill_list_kernel(const __grid
 
 // Queries [tokens][heads][head_dim] seen as 3-D (head_dim, heads, tokens); a box is 8
 // tokens x 64 dims of one head, landing as one swizzled 64-column block of an 8-row group.
-bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16, int head_dim) {
+bool make_query_map_uncached(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16,
+                             int head_dim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
@@ -653,6 +661,12 @@ bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t toke
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q),
             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_query_map(CUtensorMap* m, const void* q, uint32_t heads, uint32_t tokens, bool bf16, int head_dim) {
+  return cached_map(m, MapKey{q, tokens, heads, 4, bf16 ? 2 : 1, head_dim}, [&](CUtensorMap* out) {
+    return make_query_map_uncached(out, q, heads, tokens, bf16, head_dim);
+  });
 }
 
 template <typename T, int D>

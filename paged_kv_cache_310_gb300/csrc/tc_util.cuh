@@ -44,9 +44,22 @@ struct ItemCursor {
   }
 };
 
-// Bounded wait that also gives up when another role has aborted.
+// Bounded wait that also gives up when another role has aborted; limit_ns is the
+// launch's wait limit (normally kWaitLimitNs).
 __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err) {
+                                          int* err, uint64_t limit_ns) {
+  if (limit_ns < kPollBelowNs) {  // a short limit: probe without suspending, clock every round
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_test_wait(bar, parity)) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        set_error(err, kErrTimeout);
+        return false;
+      }
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -54,7 +67,7 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       set_error(err, kErrTimeout);
       return false;
@@ -189,12 +202,50 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoding a tiled TMA map is host work a decode call repeated for each of its maps
+// on every call.  A map depends only on what is in its key, so the last few encoded
+// on this host thread are kept and handed out again (a serving loop reuses the same
+// pools and a few q buffers).  `kind` tells the map layouts apart.
+struct MapKey {
+  const void* base;
+  uint64_t rows;
+  uint32_t box_rows;
+  int kind, dtype, head_dim;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && box_rows == o.box_rows && kind == o.kind && dtype == o.dtype &&
+           head_dim == o.head_dim;
+  }
+};
+
+template <typename Encode>
+bool cached_map(CUtensorMap* m, const MapKey& key, Encode encode) {
+  struct Entry {
+    CUtensorMap map;
+    MapKey key;
+    bool used;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i)
+    if (cache[i].used && cache[i].key == key) {
+      *m = cache[i].map;
+      return true;
+    }
+  if (!encode(m)) return false;
+  cache[next].map = *m;
+  cache[next].key = key;
+  cache[next].used = true;
+  next = (next + 1) % kEntries;
+  return true;
+}
+
 // Pool of rows of head_dim (64 or 128) 16-bit elements seen as 4-D: (64 columns,
 // 8 rows, 64-column blocks, 8-row groups) with byte strides (-, row, 128, 8 rows).  A
 // box of (64, 8, head_dim/64, bs/8) is one block's tile for one KV head, landing as
 // [group][column block][row][64 columns].
-bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16,
-                   int head_dim) {
+bool make_pool_map_uncached(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16,
+                            int head_dim) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows % 8 || (head_dim != 64 && head_dim != 128)) return false;
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(head_dim) * 2, blocks = head_dim / 64;
@@ -206,6 +257,13 @@ bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t blo
             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16,
+                   int head_dim) {
+  return cached_map(m, MapKey{base, rows, block_size, 1, bf16 ? 2 : 1, head_dim}, [&](CUtensorMap* out) {
+    return make_pool_map_uncached(out, base, rows, block_size, bf16, head_dim);
+  });
 }
 
 int sm_count() {

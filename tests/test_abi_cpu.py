@@ -58,7 +58,8 @@ def test_workspace_sizes(lib):
     assert _ws(lib, 64, 32, 2048, d, path=tensor, part=8192) == 0  # partitions <= 4096 on tensor cores
     assert _ws(lib, 64, 32, 2048, d, part=100) == 0       # invalid partition size
     assert _ws(lib, 64, 30, 2048, d) == 0                 # heads not a multiple of kv heads
-    assert _ws(lib, 4, 8, 2048, _desc(dtype=pkv.F32), path=tensor) == 0  # f32 has no tensor path
+    assert _ws(lib, 4, 8, 2048, _desc(dtype=pkv.F32), path=tensor) > 0   # f32: the tf32 kernel's work list
+    assert _ws(lib, 4, 8 * 9, 2048, _desc(dtype=pkv.F32), path=tensor) == 0  # f32 groups above 8: none
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -146,8 +147,14 @@ def test_plan_reports_path_partitions_and_launches(lib):
     assert pkv.paged_attention_plan(128, 8, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # 64-token blocks
     k32b64 = torch.empty((1, 8, 64, 128), dtype=torch.float32)
     assert pkv.paged_attention_plan(32, 8, 2048, k32b64)["path"] == pkv.PATH_CUDA_CORE
-    with pytest.raises(pkv.PagedKVError):   # f32 has no tensor-core path
-        pkv.paged_attention_plan(64, 8, 2048, k32, path=pkv.PATH_TENSOR_CORE)
+    # f32: CUDA cores below 4 query heads per KV head, the tf32 tensor-core kernel from 4
+    # to 8, nothing above 8
+    assert pkv.paged_attention_plan(64, 8, 2048, k32, path=pkv.PATH_TENSOR_CORE)["path"] == pkv.PATH_TENSOR_CORE
+    assert pkv.paged_attention_plan(64, 32, 2048, k32)["path"] == pkv.PATH_TENSOR_CORE   # group 4
+    assert pkv.paged_attention_plan(64, 64, 2048, k32)["path"] == pkv.PATH_TENSOR_CORE   # group 8
+    assert pkv.paged_attention_plan(64, 24, 2048, k32)["path"] == pkv.PATH_CUDA_CORE     # group 3
+    with pytest.raises(pkv.PagedKVError):
+        pkv.paged_attention_plan(64, 72, 2048, k32, path=pkv.PATH_TENSOR_CORE)          # group 9
     with pytest.raises(pkv.PagedKVError):   # f32 at group 16: above the CUDA-core path's 8
         pkv.paged_attention_plan(4, 128, 2048, k32b64)
     assert pkv.paged_attention_plan(4, 128, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # bf16 at group 16

@@ -34,3 +34,11 @@ def test_recorded_traffic_matches_only_its_own_workload_and_partition():
     assert bench.recorded_traffic("tensor_core", e["workload"] + " [with block_size=64]",
                                   e["partition_tokens"]) is None
     assert bench.recorded_traffic("cuda_core", e["workload"], e["partition_tokens"]) is None
+
+
+def test_f32_tensor_core_decode_is_looked_up_under_its_own_sources():
+    import torch
+    assert bench.traffic_path(2, torch.float32) == "tensor_core_f32"
+    assert bench.traffic_path(2, torch.bfloat16) == "tensor_core"
+    assert bench.traffic_path(1, torch.float32) == "cuda_core"
+    assert "decode_tc32.cu" in bench.KERNEL_SOURCES["tensor_core_f32"]

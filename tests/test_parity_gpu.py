@@ -29,7 +29,7 @@ PATH_IDS = {pkv.PATH_CUDA_CORE: "cuda_core", pkv.PATH_TENSOR_CORE: "tensor_core"
 def supported(path, dtype, head_dim, group):
     """The library's supported set per path (include/pagedkv.h)."""
     if path == pkv.PATH_TENSOR_CORE:
-        return dtype in (torch.float16, torch.bfloat16) and head_dim in (64, 128) and group <= 16
+        return head_dim in (64, 128) and group <= (8 if dtype == torch.float32 else 16)
     return group <= 8
 
 
@@ -138,6 +138,10 @@ CASES = [
     # 64-token blocks: a block spans two CUDA-core stages and half a tensor-core chunk
     ("bf16", 128, 64, 16, 4, 1500, 0), ("f16", 64, 64, 8, 8, 700, 256), ("f32", 128, 64, 4, 2, 900, 128),
     ("bf16", 128, 64, 8, 1, 130, 128), ("f32", 64, 64, 2, 2, 2500, 0),
+    # f32 with grouped query heads (the tf32 tensor-core kernel from 4 per KV head)
+    ("f32", 128, 16, 64, 8, 1500, 512), ("f32", 64, 16, 16, 2, 1000, 0), ("f32", 128, 8, 7, 1, 600, 256),
+    ("f32", 128, 32, 40, 8, 2100, 0), ("f32", 64, 8, 24, 6, 900, 128), ("f32", 128, 64, 8, 1, 700, 0),
+    ("f32", 64, 32, 32, 8, 3000, 384), ("f32", 128, 16, 5, 5, 1, 0),
 ]
 
 
