@@ -58,8 +58,9 @@
  *  - Supported set: dtype f32, f16, bf16 (q, k, v, caches share it); out dtype
  *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
  *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
- *    up to 8 on the CUDA-core decode path and up to 16 on the tensor-core paths
- *    (f16/bf16, head_dim 64 or 128).
+ *    up to 8 on the CUDA-core decode path; on the tensor-core decode path up to 16
+ *    for f16/bf16 and up to 8 for f32 (tf32 MMAs on split operands, within the f32
+ *    tolerance); prefill on tensor cores for f16/bf16, groups up to 16.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -94,7 +95,8 @@ typedef struct {
 } pkv_cache_desc;
 
 /* Decode path selection and split-K partition size (NULL config = automatic: tensor
- * cores for f16/bf16 with groups <= 16, CUDA cores otherwise, i.e. for f32). */
+ * cores for f16/bf16 with groups <= 16 and for f32 with groups 5 to 8, CUDA cores
+ * otherwise). */
 typedef enum { PKV_PATH_AUTO = 0, PKV_PATH_CUDA_CORE = 1, PKV_PATH_TENSOR_CORE = 2 } pkv_path;
 
 typedef struct {

@@ -105,10 +105,11 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   // Tensor cores wherever they apply to 16-bit caches: at G >= 2 QK and PV are real
   // contractions, and at G = 1 the persistent TMA/tcgen05 kernel still streams K/V
   // slightly faster (0.977 vs 0.922 of copy bandwidth on a 64 x 32-head bf16 batch).
-  // f32 caches take the tf32 kernel from 4 query heads per KV head; below that the
-  // CUDA-core kernel streams at copy bandwidth with no extra conversion work.
+  // f32 caches take the tf32 kernel from 5 query heads per KV head (at 8: 0.82 of copy
+  // bandwidth against 0.36 on CUDA cores, head_dim 128); up to 4 the CUDA-core kernel
+  // streams faster (0.92 against 0.84 at 4) with no conversion work.
   if (path == PKV_PATH_AUTO)
-    path = tc_ok && (c->dtype != PKV_F32 || group >= 4) ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
+    path = tc_ok && (c->dtype != PKV_F32 || group >= 5) ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
   if (path == PKV_PATH_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED,
                 "tensor-core path needs head_dim 64 or 128 and group <= 16 (<= 8 for f32) (group %d)", group);

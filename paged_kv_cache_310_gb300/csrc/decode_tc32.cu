@@ -60,7 +60,7 @@ constexpr int kStageTok = 64;   // tokens per landing stage
 constexpr int kPiece = 32;      // tokens per V^T piece in tensor memory (K of one PV group)
 constexpr int kN = 16;          // MMA N: [x 0-7 | x_lo 0-7]
 constexpr int kMaxG = 8;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;  // two per TMEM lane quarter
 constexpr uint32_t kTmemCols = 512;
 
 template <int GM>
@@ -69,8 +69,10 @@ struct Roles32 {
   static constexpr int kHeads = GM / kSplit;
   static constexpr int kSoftmaxThreads = 128 * kSplit;
   static constexpr int kThreads = kSoftmaxThreads + 32 * (kConvWarps + 3);
+  static constexpr int kConv2 = 11 + 4 * (kSplit - 1);  // first warp of the second converter set
 };
-// warps: 0-3 softmax, 4-7 converters, 8 K producer, 9 V producer, 10 MMA, 11-14 softmax
+// warps: 0-3 softmax, 4-7 converters (first set), 8 K producer, 9 V producer, 10 MMA,
+// then 11-14 softmax (from G = 4), then four more converters (second set)
 constexpr int kWarpKProd = 8, kWarpVProd = 9, kWarpMma = 10;
 constexpr int kVBufs = kChunk / kPiece;  // V^T piece buffers in tensor memory: one whole chunk
 
@@ -78,19 +80,24 @@ template <int D>
 struct Layout32 {
   static constexpr int kBlocks = D / 32;                 // 128-byte column blocks of a row
   static constexpr int kGroupBytes = 8 * D * 4;          // 8 token rows
-  static constexpr int kKSlotBytes = kChunk * D * 4;     // K of one chunk: 64 KB at D = 128
-  static constexpr int kKSlots = 256 / D;                // 2 (128 KB) or 4 (128 KB)
+  // K lands in units of 128 tokens x 64 dimensions (a chunk has D / 64 of them), each
+  // the A operand of QK for its dimensions; three units in a ring (1.5 chunks at D =
+  // 128, 3 at 64).  V lands in 64-token stages, 96 KB of them.
+  static constexpr int kKUnitBytes = kChunk * 64 * 4;    // 32 KB
+  static constexpr int kKUnitsPerChunk = D / 64;
+  static constexpr int kKSlots = 3;
+  static constexpr int kKUnitGroupBytes = 8 * 64 * 4;   // 8 token rows of a unit: 2 KB
   static constexpr int kVStageBytes = kStageTok * D * 4;  // 32 KB at D = 128
-  static constexpr int kVStages = 256 / D;               // 2 (64 KB) or 4 (64 KB)
+  static constexpr int kVStages = 3 * 128 / D;           // 96 KB
   static constexpr int kQBytes = kN * D * 4;             // [q | q_lo] of one item
   static constexpr int kPBytes = kN * kChunk * 4;        // [p | p_lo] of one chunk
-  static constexpr int kOffV = kKSlots * kKSlotBytes;
+  static constexpr int kOffV = kKSlots * kKUnitBytes;
   static constexpr int kOffQ = kOffV + kVStages * kVStageBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  // kfull, kempty per K slot; vfull, vempty per V stage; vtfull, vtfree per V^T buffer;
-  // qready, qfree, sfull, sfree, pfull, ofull, ofree pairs; ktfull, ktfree, drain
-  static constexpr int kNumBars = 2 * kKSlots + 2 * kVStages + 2 * kVBufs + 7 * 2 + 3;
+  // kfull, kempty per K slot; vfull, vempty per V stage; qready, qfree, sfull, sfree,
+  // pfull, ofull, ofree pairs; ktfull, ktfree, vtready, drain
+  static constexpr int kNumBars = 2 * kKSlots + 2 * kVStages + 7 * 2 + 4;
   static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;
   static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;
@@ -104,9 +111,9 @@ struct Layout32 {
 };
 
 struct Bars32 {
-  uint64_t *kfull, *kempty, *vfull, *vempty, *vtfull, *vtfree;
+  uint64_t *kfull, *kempty, *vfull, *vempty;
   uint64_t *qready, *qfree, *sfull, *sfree, *pfull, *ofull, *ofree;
-  uint64_t *ktfull, *ktfree, *drain;
+  uint64_t *ktfull, *ktfree, *vtready, *drain;
 };
 
 template <int D>
@@ -118,9 +125,7 @@ __device__ __forceinline__ Bars32 carve32(unsigned char* smem) {
   r.kempty = r.kfull + L::kKSlots;
   r.vfull = r.kempty + L::kKSlots;
   r.vempty = r.vfull + L::kVStages;
-  r.vtfull = r.vempty + L::kVStages;
-  r.vtfree = r.vtfull + kVBufs;
-  r.qready = r.vtfree + kVBufs;
+  r.qready = r.vempty + L::kVStages;
   r.qfree = r.qready + 2;
   r.sfull = r.qfree + 2;
   r.sfree = r.sfull + 2;
@@ -129,7 +134,8 @@ __device__ __forceinline__ Bars32 carve32(unsigned char* smem) {
   r.ofree = r.ofull + 2;
   r.ktfull = r.ofree + 2;
   r.ktfree = r.ktfull + 1;
-  r.drain = r.ktfree + 1;
+  r.vtready = r.ktfree + 1;
+  r.drain = r.vtready + 1;
   return r;
 }
 
@@ -236,15 +242,11 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKS; ++i) {
       mbar_init(&bars.kfull[i], 1);
-      mbar_init(&bars.kempty[i], 1);  // the chunk's QK completed
+      mbar_init(&bars.kempty[i], 1);  // the QK of the unit's chunk completed
     }
     for (int i = 0; i < kVS; ++i) {
       mbar_init(&bars.vfull[i], 1);
       mbar_init(&bars.vempty[i], kConvWarps);  // converted into tensor memory
-    }
-    for (int i = 0; i < kVBufs; ++i) {
-      mbar_init(&bars.vtfull[i], kConvWarps);
-      mbar_init(&bars.vtfree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.qready[i], kConvWarps);
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
     }
     mbar_init(bars.ktfull, kConvWarps);
     mbar_init(bars.ktfree, 1);
+    mbar_init(bars.vtready, kConvWarps);
     *abort_flag = 0;
     *kissued_slot = 0;
     *vissued_slot = 0;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
 
   if (warp == kWarpKProd || warp == kWarpVProd) {
     // ============================ TMA producers ============================
-    // K: one slot per 128-token chunk (the A operand of QK); V: 64-token stages.
+    // K: units of 128 tokens x 64 dimensions (the A operand of QK); V: 64-token stages.
     const bool is_k = warp == kWarpKProd;
     const CUtensorMap* map = is_k ? &a.tk : &a.tv;
     if (lane == 0) prefetch_tensormap(map);
@@ -287,7 +290,8 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
     unsigned char* ring = smem + (is_k ? 0 : L::kOffV);
     const int ring_n = is_k ? kKS : kVS;
     const int unit_tok = is_k ? kChunk : kStageTok;
-    const uint32_t unit_bytes = is_k ? L::kKSlotBytes : L::kVStageBytes;
+    const uint32_t unit_bytes = is_k ? L::kKUnitBytes : L::kVStageBytes;
+    const int row_bytes = is_k ? 64 * 4 : D * 4;  // bytes a token row of a unit holds
     int* issued_slot = is_k ? kissued_slot : vissued_slot;
     const uint64_t pol = policy_evict_first();
     const int bs = p.block_size;
@@ -300,10 +304,11 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
       const Item32 it = unpack32(cur.cur, p.part_tokens);
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k) {
-        const int nunits = is_k ? 1 : chunk_stages(chunk_rows(it, k));
+        const int nunits = is_k ? L::kKUnitsPerChunk : chunk_stages(chunk_rows(it, k));
         for (int h = 0; h < nunits; ++h, ++u) {
           const int slot = u % ring_n;
-          const int lb = (it.t0 + k * kChunk + h * kStageTok) / bs + lane;  // this lane's logical block
+          // K unit h: the chunk's tokens, dimensions 64 h ..; V stage h: tokens 64 h ..
+          const int lb = (it.t0 + k * kChunk + (is_k ? 0 : h * kStageTok)) / bs + lane;  // this lane's block
           const bool live = lane < blocks_per_unit && lb * bs < it.t0 + it.ntok;
           int b = live ? (lb < p.max_blocks_per_seq ? table[lb] : -1) : 0;
           if (lane == 0) {
@@ -322,20 +327,23 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
               }
               row = (b * p.num_kv_heads + it.g) * bs;
             }
-            tma_load_4d(ring + slot * unit_bytes + lane * bs * (D * 4), map, row / 8, &full[slot], pol);
+            tma_load_4d_zw(ring + slot * unit_bytes + lane * bs * row_bytes, map, is_k ? 2 * h : 0, row / 8,
+                           &full[slot], pol);
           }
           if (lane == 0) *issued_slot = u + 1;
         }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= R::kConv2) {
     // ============================ converters ============================
+    // Two warps per TMEM lane quarter: set ch = 0 or 1 takes half of each piece's tokens,
+    // half of K's column blocks and half of q.
     const int quarter = warp & 3;
+    const int ch = warp >= R::kConv2 ? 1 : 0;
     const int r = quarter * 32 + lane;  // TMEM lane: token row (K_lo) or dimension (V^T)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int kc = 0;           // chunks whose K_lo was written
     int vst = 0;          // V stages consumed
-    uint32_t vused = 0, vpar = 0;  // per V^T buffer (bit b): used before / number of uses is odd
     int j = 0;            // items whose q was converted
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
       if (j >= 2 && !wait(&bars.qfree[qb], ((j >> 1) - 1) & 1)) return false;
       unsigned char* qbuf = smem + L::kOffQ + qb * L::kQBytes;
       const float* qg = static_cast<const float*>(p.q) + (static_cast<size_t>(it.s) * p.num_q_heads + it.g * G) * D;
-      for (int e = r; e < kMaxG * D; e += 128) {
+      for (int e = r + 128 * ch; e < kMaxG * D; e += 256) {
         const int h = e / D, d = e % D;
         const float x = h < G ? qg[h * D + d] : 0.f;
         *reinterpret_cast<float*>(qbuf + bmat_off(h, d, D)) = x;
@@ -362,17 +370,20 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
     // K_lo of one chunk -> tensor memory, lane = token (the raw K stays in its slot,
     // where QK reads it as the other A operand)
     auto convert_k = [&]() -> bool {
-      const int slot = kc % kKS;
+      const int u0 = kc * L::kKUnitsPerChunk;  // the chunk's first K unit
       if (kc >= 1 && !wait(bars.ktfree, (kc - 1) & 1)) return false;
-      if (!wait(&bars.kfull[slot], (kc / kKS) & 1)) return false;
+      for (int h = 0; h < L::kKUnitsPerChunk; ++h)
+        if (!wait(&bars.kfull[(u0 + h) % kKS], ((u0 + h) / kKS) & 1)) return false;
       tc_fence_after();
-      const unsigned char* src = smem + slot * L::kKSlotBytes;
 #pragma unroll
-      for (int cb = 0; cb < L::kBlocks; ++cb) {
+      for (int cb = ch * L::kBlocks / 2; cb < (ch + 1) * L::kBlocks / 2; ++cb) {
+        // column block cb: block cb % 2 of unit cb / 2 ([8-row group][2 blocks][8 rows][128 B])
+        const unsigned char* src = smem + ((u0 + cb / 2) % kKS) * L::kKUnitBytes + (r >> 3) * L::kKUnitGroupBytes +
+                                   (cb & 1) * 1024 + (r & 7) * 128;
         float lo[32];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          const float4 v = *reinterpret_cast<const float4*>(src + stage_off<D>(r, cb, jj));
+          const float4 v = *reinterpret_cast<const float4*>(src + ((jj ^ (r & 7)) << 4));
           lo[4 * jj] = tf32_low(v.x);
           lo[4 * jj + 1] = tf32_low(v.y);
           lo[4 * jj + 2] = tf32_low(v.z);
@@ -387,36 +398,45 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
       ++kc;
       return true;
     };
-    // piece pp (32 tokens) of the current V chunk -> V^T buffer pp, lane = dimension:
-    // V^T at kColV + 64 pp, V_lo^T at kColV + 64 pp + 32; rows past the context end as 0
-    auto convert_v = [&](int rows, int pp) -> bool {
-      const int stg = vst + pp / 2;  // landing stage holding the piece
-      if (((vused >> pp) & 1) && !wait(&bars.vtfree[pp], ((vpar >> pp) & 1) ^ 1)) return false;
-      if (!wait(&bars.vfull[stg % kVS], (stg / kVS) & 1)) return false;
+    // V of one chunk -> tensor memory, lane = dimension, in one pass: V^T of piece pp
+    // (32 tokens) at kColV + 64 pp, V_lo^T at kColV + 64 pp + 32, rows past the context
+    // end as 0.  The buffers are free once the previous chunk's PV completed (its O is
+    // ready); set ch converts pieces 2 ch and 2 ch + 1, which sit in landing stage ch.
+    int vc = 0;  // chunks of V converted
+    auto convert_v = [&](int rows) -> bool {
+      const int nst = chunk_stages(rows), np = chunk_pieces(rows);
+      if (vc >= 1 && !wait(&bars.ofull[(vc - 1) & 1], ((vc - 1) >> 1) & 1)) return false;
+      for (int h = 0; h < nst; ++h)
+        if (!wait(&bars.vfull[(vst + h) % kVS], ((vst + h) / kVS) & 1)) return false;
       tc_fence_after();
-      if (r < D) {
-        const unsigned char* src = smem + L::kOffV + (stg % kVS) * L::kVStageBytes;
+      if (r < D && 2 * ch < np) {  // warp-uniform
+        const unsigned char* src = smem + L::kOffV + ((vst + ch) % kVS) * L::kVStageBytes;
         const int cb = r >> 5, jj = (r & 31) >> 2, e = (r & 3) << 2;
-        float x[32], lo[32];
 #pragma unroll
-        for (int i = 0; i < kPiece; ++i) {
-          const int t = pp * kPiece + i;  // token within the chunk
-          x[i] = t < rows ? *reinterpret_cast<const float*>(src + stage_off<D>(t % kStageTok, cb, jj) + e) : 0.f;
-          lo[i] = tf32_low(x[i]);
+        for (int q = 0; q < 2; ++q) {
+          const int pp = 2 * ch + q;
+          if (pp < np) {
+            float x[kPiece], lo[kPiece];
+#pragma unroll
+            for (int i = 0; i < kPiece; ++i) {
+              const int t = pp * kPiece + i;  // token within the chunk (row t % 64 of stage ch)
+              x[i] = t < rows ? *reinterpret_cast<const float*>(src + stage_off<D>(t % kStageTok, cb, jj) + e) : 0.f;
+              lo[i] = tf32_low(x[i]);
+            }
+            tmem_store32_nowait(lane_base + L::kColV + 64 * pp, x);
+            tmem_store32_nowait(lane_base + L::kColV + 64 * pp + 32, lo);
+          }
         }
-        tmem_store32_nowait(lane_base + L::kColV + 64 * pp, x);
-        tmem_store32_nowait(lane_base + L::kColV + 64 * pp + 32, lo);
         tmem_store_wait();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars.vtfull[pp]);
-        // a stage is done with after its second piece, or after the chunk's last
-        if ((pp & 1) || pp == chunk_pieces(rows) - 1) mbar_arrive(&bars.vempty[stg % kVS]);
+        mbar_arrive(bars.vtready);
+        for (int h = 0; h < nst; ++h) mbar_arrive(&bars.vempty[(vst + h) % kVS]);
       }
-      vused |= 1u << pp;
-      vpar ^= 1u << pp;
+      vst += nst;
+      ++vc;
       return true;
     };
 
@@ -443,16 +463,14 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
       const Item32 it = unpack32(cur.cur, p.part_tokens);
       for (int k = 0; k < it.nchunks && ok; ++k) {
         ok = next_k();
-        const int rows = chunk_rows(it, k), np = chunk_pieces(rows);
-        for (int pp = 0; pp < np && ok; ++pp) ok = convert_v(rows, pp);
-        vst += chunk_stages(rows);
+        if (ok) ok = convert_v(chunk_rows(it, k));
       }
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ============================ MMA issuer ============================
     constexpr uint32_t idesc = idesc_tf32(128, kN);
-    const uint64_t dk0 = smem_desc(smem_addr(smem), 16, L::kGroupBytes, kLayoutSwizzle128);
+    const uint64_t dk0 = smem_desc(smem_addr(smem), 16, L::kKUnitGroupBytes, kLayoutSwizzle128);
     const uint64_t dq0 = smem_desc(smem_addr(smem + L::kOffQ), 16, L::kBlocks * 1024, kLayoutSwizzle128);
     const uint64_t dp0 = smem_desc(smem_addr(smem + L::kOffP), 16, (kChunk / 32) * 1024, kLayoutSwizzle128);
     ItemCursor qcur, pcur;
@@ -460,8 +478,7 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
     pcur.init(p.work_list, num_items);
     int qk = 0, qj = 0, qc = 0;
     int qn = qcur.valid() ? unpack32(qcur.cur, p.part_tokens).nchunks : 0;
-    int pk = 0, pc = 0, pp = 0;  // PV: chunk within item, global chunk, piece
-    uint32_t vpar = 0;  // per V^T buffer (bit b): number of uses so far is odd
+    int pk = 0, pc = 0;  // PV: chunk within its item, global chunk
     int pn = qn;
     int prows = pcur.valid() ? chunk_rows(unpack32(pcur.cur, p.part_tokens), 0) : 0;
     uint64_t idle_since = global_timer_ns();
@@ -469,55 +486,51 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
       bool progressed = false;
       const int sb = qc & 1, pb = pc & 1;
       // bit 0: K_lo of chunk qc in tensor memory (its raw K landed before), 1: S[qc & 1]
-      // free, 2: P of chunk pc written, 3: V^T piece pp of chunk pc in tensor memory
+      // free, 2: P of chunk pc written, 3: V^T of chunk pc in tensor memory
       const uint32_t seen = __shfl_sync(0xffffffffu,
           mbar_test_wait4(bars.ktfull, qc & 1, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
-                          (pc >> 1) & 1, &bars.vtfull[pp], (vpar >> pp) & 1), 0);
+                          (pc >> 1) & 1, bars.vtready, pc & 1), 0);
       if (pc < qc && (seen & 4) && (seen & 8) &&
-          (pp > 0 || pc < 2 || __all_sync(0xffffffffu, mbar_test_wait(&bars.ofree[pb], ((pc >> 1) - 1) & 1)))) {
-        const uint64_t dp = dp0 + ((pb * L::kPBytes + pp * 1024) >> 4);
-        const uint32_t vcol = tmem + L::kColV + 64 * pp;
-        const bool last_piece = pp == chunk_pieces(prows) - 1;
+          (pc < 2 || __all_sync(0xffffffffu, mbar_test_wait(&bars.ofree[pb], ((pc >> 1) - 1) & 1)))) {
+        const int np = chunk_pieces(prows);
         tc_fence_after();
         if (elect_one()) {
+          for (int pp = 0; pp < np; ++pp) {
+            const uint64_t dp = dp0 + ((pb * L::kPBytes + pp * 1024) >> 4);
+            const uint32_t vcol = tmem + L::kColV + 64 * pp;
 #pragma unroll
-          for (int kk = 0; kk < kPiece / 8; ++kk)
-            mma_tf32_tmem_a(tmem + L::kColO + pb * kN, vcol + 8 * kk, dp + ((kk * 32) >> 4), idesc,
-                            pp > 0 || kk > 0);
+            for (int kk = 0; kk < kPiece / 8; ++kk)
+              mma_tf32_tmem_a(tmem + L::kColO + pb * kN, vcol + 8 * kk, dp + ((kk * 32) >> 4), idesc,
+                              pp > 0 || kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < kPiece / 8; ++kk)
-            mma_tf32_tmem_a(tmem + L::kColO + pb * kN, vcol + 32 + 8 * kk, dp + ((kk * 32) >> 4), idesc, true);
-          mma_commit(&bars.vtfree[pp]);
-          if (last_piece) mma_commit(&bars.ofull[pb]);
+            for (int kk = 0; kk < kPiece / 8; ++kk)
+              mma_tf32_tmem_a(tmem + L::kColO + pb * kN, vcol + 32 + 8 * kk, dp + ((kk * 32) >> 4), idesc, true);
+          }
+          mma_commit(&bars.ofull[pb]);  // also frees the V^T buffers for the next chunk
         }
         __syncwarp();
-        vpar ^= 1u << pp;
-        if (!last_piece) {
-          ++pp;
-        } else {
-          pp = 0;
-          ++pc;
-          if (++pk == pn) {
-            pk = 0;
-            pcur.advance();
-            pn = pcur.valid() ? unpack32(pcur.cur, p.part_tokens).nchunks : 0;
-          }
-          prows = pcur.valid() ? chunk_rows(unpack32(pcur.cur, p.part_tokens), pk) : 0;
+        ++pc;
+        if (++pk == pn) {
+          pk = 0;
+          pcur.advance();
+          pn = pcur.valid() ? unpack32(pcur.cur, p.part_tokens).nchunks : 0;
         }
+        prows = pcur.valid() ? chunk_rows(unpack32(pcur.cur, p.part_tokens), pk) : 0;
         progressed = true;
       }
       if (qcur.valid() && (seen & 1) && (qc < 2 || (seen & 2)) &&
           (qk > 0 || __all_sync(0xffffffffu, mbar_test_wait(&bars.qready[qj & 1], (qj >> 1) & 1)))) {
-        const int slot = qc % kKS;
-        const uint64_t dk = dk0 + ((slot * L::kKSlotBytes) >> 4);
+        const int u0 = qc * L::kKUnitsPerChunk;  // the chunk's first K unit
         const uint64_t dq = dq0 + (((qj & 1) * L::kQBytes) >> 4);
         const bool last = qk == qn - 1;
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 8; ++kk) {
-            const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            mma_tf32(tmem + L::kColS + sb * kN, dk + off, dq + off, idesc, kk > 0);
+            // dimensions 8 kk ..: unit kk / 8, its column block (kk / 4) % 2, 32 bytes per step
+            const uint32_t ko = (((u0 + kk / 8) % kKS) * L::kKUnitBytes + ((kk >> 2) & 1) * 1024 + (kk & 3) * 32) >> 4;
+            const uint32_t qo = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            mma_tf32(tmem + L::kColS + sb * kN, dk0 + ko, dq + qo, idesc, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 8; ++kk) {
@@ -526,7 +539,7 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
           }
           mma_commit(&bars.sfull[sb]);
           mma_commit(bars.ktfree);
-          mma_commit(&bars.kempty[slot]);
+          for (int h = 0; h < L::kKUnitsPerChunk; ++h) mma_commit(&bars.kempty[(u0 + h) % kKS]);
           if (last) mma_commit(&bars.qfree[qj & 1]);
         }
         __syncwarp();
@@ -759,23 +772,25 @@ __global__ void __launch_bounds__(Roles32<GM>::kThreads, 1) decode_tc32_kernel(c
 // blocks, 8-row groups), byte strides (row, 128, 8 rows); a box of (32, 8, D/32, bs/8)
 // is one block's tile of one KV head, landing as [group][block][8 rows][128 B].
 bool make_pool_map32_uncached(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size,
-                              int head_dim) {
+                              int head_dim, uint32_t box_blocks) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows % 8 || (head_dim != 64 && head_dim != 128)) return false;
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(head_dim) * 4, blocks = head_dim / 32;
   cuuint64_t dims[4] = {32, 8, blocks, rows / 8};
   cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
-  cuuint32_t box[4] = {32, 8, static_cast<cuuint32_t>(blocks), block_size / 8};
+  cuuint32_t box[4] = {32, 8, box_blocks, block_size / 8};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_pool_map32(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, int head_dim) {
-  return cached_map(m, MapKey{base, rows, block_size, 3, 0, head_dim}, [&](CUtensorMap* out) {
-    return make_pool_map32_uncached(out, base, rows, block_size, head_dim);
-  });
+bool make_pool_map32(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, int head_dim,
+                     uint32_t box_blocks) {
+  return cached_map(m, MapKey{base, rows, block_size, 3 + 16 * static_cast<int>(box_blocks), 0, head_dim},
+                    [&](CUtensorMap* out) {
+                      return make_pool_map32_uncached(out, base, rows, block_size, head_dim, box_blocks);
+                    });
 }
 
 template <int D, int GM>
@@ -803,8 +818,8 @@ cudaError_t launch_decode_tc32(const DecodeParams& p, int grid, cudaStream_t str
   Tc32Args args;
   args.p = p;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_pool_map32(&args.tk, p.k_cache, pool_rows, p.block_size, p.head_dim) ||
-      !make_pool_map32(&args.tv, p.v_cache, pool_rows, p.block_size, p.head_dim))
+  if (!make_pool_map32(&args.tk, p.k_cache, pool_rows, p.block_size, p.head_dim, 2) ||
+      !make_pool_map32(&args.tv, p.v_cache, pool_rows, p.block_size, p.head_dim, p.head_dim / 32))
     return cudaErrorInvalidValue;
   return p.head_dim == 64 ? launch32_g<64>(args, grid, stream) : launch32_g<128>(args, grid, stream);
 }

@@ -235,6 +235,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Tiled 4-D TMA load of the box at (0, 0, z, w).
+__device__ __forceinline__ void tma_load_4d_zw(void* dst, const CUtensorMap* map, int z, int w, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(z), "r"(w), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Tiled 3-D TMA load of the box at (x, y, z).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar, uint64_t policy) {
