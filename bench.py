@@ -54,6 +54,8 @@ def parse():
                     help="override the workload's query heads (a multiple of its KV heads: another group size)")
     ap.add_argument("--dtype", default="", choices=["", "f32", "f16", "bf16"],
                     help="override the workload's cache dtype")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="override the workload's batch size (workloads 2, 3 and 5; a smaller profiling case)")
     ap.add_argument("--identity-tables", action="store_true",
                     help="physical blocks in logical order (contiguous sequences): the indirection A/B")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
@@ -494,7 +496,8 @@ def main():
     path = {"auto": pkv.PATH_AUTO, "cuda_core": pkv.PATH_CUDA_CORE, "tensor_core": pkv.PATH_TENSOR_CORE}[args.path]
     # every rank decodes its own batch of the same workload shape (independent replicas)
     overrides = {k: v for k, v in (("block_size", args.block_size), ("head_dim", args.head_dim),
-                                   ("num_q_heads", args.num_q_heads), ("dtype", args.dtype)) if v}
+                                   ("num_q_heads", args.num_q_heads), ("dtype", args.dtype),
+                                   ("num_seqs", args.num_seqs)) if v}
     w = workloads.make_workload(args.config, canary=False, pool_device=dev, shuffle=not args.identity_tables,
                                 **overrides)
     g = w.to(dev)
