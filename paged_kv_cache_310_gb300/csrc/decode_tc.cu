@@ -23,7 +23,7 @@
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
 // head) that work_list_kernel sorts longest first and the CTAs take in snake order;
 // the kernel is launched as a programmatic dependent of that list kernel.  224 threads
-// (352 from 4 query heads per KV head) in five roles:
+// (352 from 4 query heads per KV head, 608 at 16) in five roles:
 //  * warp 4, producer of Q and K: per 128-token chunk, one lane per physical block
 //    reads the block id (before waiting for a free stage, hiding its latency) and
 //    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
@@ -38,9 +38,9 @@
 //    elected lane issues PV for the oldest chunk whose probabilities are in shared
 //    memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed; commits
 //    release the ring stages and signal the softmax warps.
-//  * warps 0-3, and from G = 4 also warps 7-10, softmax (thread t = TMEM lane t; a warp
-//    reads the lane quarter of its index mod 4, so with eight warps two share each
-//    quarter and take half of the heads each): read S row t (token t, its heads), vote
+//  * warps 0-3, and from G = 4 also warps 7-10 (from 16, 7-18), softmax (thread t = TMEM
+//    lane t; a warp reads the lane quarter of its index mod 4, so with eight warps two
+//    share each quarter and take half of the heads each): read S row t (token t, its heads), vote
 //    on whether any score exceeds its head's running max by more than 2^8 (if so,
 //    chunk max across the 128 tokens by a warp reduction + shared memory and an
 //    online-softmax rescale), probabilities split into two parts rounded to the cache
@@ -73,16 +73,14 @@ constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 c
 constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
 
 // Roles: warps 0-3 softmax, 4 producer of Q and K, 5 MMA, 6 producer of V, and from
-// 4 query heads per KV head warps 7-10 softmax too: a warp reads the TMEM lane
-// quarter of its index mod 4, so two warps share each quarter (each 32 tokens) and
-// take half of the heads each, which halves the softmax work per thread.
-#ifndef PKV_TC_SPLIT_G16
-#define PKV_TC_SPLIT_G16 4
-#endif
+// 4 query heads per KV head warps 7-10 softmax too (from 16, warps 7-18): a warp
+// reads the TMEM lane quarter of its index mod 4, so two (four) warps share each
+// quarter (each 32 tokens) and take half (a quarter) of the heads each, which divides
+// the softmax work per thread.
 template <int GM>
 struct TcRoles {
-  // softmax warps per lane quarter
-  static constexpr int kSplit = GM >= 16 ? PKV_TC_SPLIT_G16 : GM >= 4 ? 2 : 1;
+  // softmax warps per lane quarter (four at 16 heads: +2.5 % at head_dim 64 over two)
+  static constexpr int kSplit = GM >= 16 ? 4 : GM >= 4 ? 2 : 1;
   static constexpr int kHeads = GM / kSplit;          // query heads per softmax thread
   static constexpr int kSoftmaxThreads = 128 * kSplit;
   static constexpr int kThreads = kSoftmaxThreads + 96;
