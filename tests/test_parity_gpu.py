@@ -201,6 +201,30 @@ def test_empty_and_single_token_sequences(path):
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_f32_empty_and_single_token_sequences(path):
+    """f32 caches with 8 query heads per KV head (the tf32 tensor-core kernel on that
+    path): an empty context gives zeros; one token gives V_0 -- exactly on CUDA cores,
+    and on tensor cores as the sum of its tf32 part and its remainder (the remainder
+    itself truncated to tf32), both weighted by exactly 1."""
+    w = workloads.random_workload(92, num_seqs=12, max_len=2, min_len=0, num_q_heads=16, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="f32")
+    assert (w.context_lens == 0).any() and (w.context_lens == 1).any()
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=path)
+    check_close(out, ref, w.dtype)
+    got = out.cpu()
+    for s in range(w.num_seqs):
+        n = int(w.context_lens[s])
+        if n == 0:
+            assert (got[s] == 0).all()
+        if n == 1:
+            b = int(w.block_tables[s, 0])
+            for h in range(w.num_q_heads):
+                # the remainder keeps 10 of its bits: within |V_0| * 2^-20
+                assert torch.allclose(got[s, h], vc[b, h // 8, 0], rtol=2.0 ** -20, atol=0)
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
 def test_head_dim_64_empty_single_and_split(path):
     """head_dim 64: empty contexts give zeros, one token gives V_0 exactly, and long
     sequences split into partitions that the merge combines."""

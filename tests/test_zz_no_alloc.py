@@ -56,6 +56,9 @@ def test_no_alloc_matches_workspace_entry_point_twice(path):
                                   head_dim=128, block_size=32, dtype="f16", canary=False),
         workloads.random_workload(310_903, num_seqs=7, max_len=1800, min_len=1, num_q_heads=16, num_kv_heads=4,
                                   head_dim=64, block_size=16, dtype="bf16", canary=False),
+        # f32 caches, 8 query heads per KV head: the tf32 kernel on the tensor-core path
+        workloads.random_workload(310_905, num_seqs=6, max_len=2000, min_len=300, num_q_heads=16, num_kv_heads=2,
+                                  head_dim=128, block_size=16, dtype="f32", canary=False),
     ]
     for w in cases:
         g = w.to("cuda")
