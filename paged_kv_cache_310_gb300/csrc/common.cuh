@@ -164,6 +164,42 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Two non-blocking probes issued back to back; bit i set when barrier i's phase has completed.
+__device__ __forceinline__ uint32_t mbar_test_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1;\n\t.reg .b32 t0, t1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "selp.b32 t0, 1, 0, q0;\n\tselp.b32 t1, 2, 0, q1;\n\tor.b32 %0, t0, t1;\n\t}"
+      : "=r"(r)
+      : "r"(smem_addr(b0)), "r"(p0), "r"(smem_addr(b1)), "r"(p1)
+      : "memory");
+  return r;
+}
+
+// Five non-blocking probes issued back to back; bit i set when barrier i's phase has completed.
+__device__ __forceinline__ uint32_t mbar_test_wait5(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                                    uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3,
+                                                    uint64_t* b4, uint32_t p4) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2, q3, q4;\n\t.reg .b32 t0, t1, t2, t3, t4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q4, [%9], %10;\n\t"
+      "selp.b32 t0, 1, 0, q0;\n\tselp.b32 t1, 2, 0, q1;\n\tselp.b32 t2, 4, 0, q2;\n\tselp.b32 t3, 8, 0, q3;\n\t"
+      "selp.b32 t4, 16, 0, q4;\n\t"
+      "or.b32 t0, t0, t1;\n\tor.b32 t2, t2, t3;\n\tor.b32 t0, t0, t4;\n\tor.b32 %0, t0, t2;\n\t}"
+      : "=r"(r)
+      : "r"(smem_addr(b0)), "r"(p0), "r"(smem_addr(b1)), "r"(p1), "r"(smem_addr(b2)), "r"(p2),
+        "r"(smem_addr(b3)), "r"(p3), "r"(smem_addr(b4)), "r"(p4)
+      : "memory");
+  return r;
+}
+
 // Four non-blocking probes issued back to back (their latencies overlap); bit i of the
 // result is set when barrier i's phase `parity_i` has completed.
 __device__ __forceinline__ uint32_t mbar_test_wait4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,

@@ -14,11 +14,11 @@
 //   S^T[128 tokens x 16] = K[128 x D dims] . Q^T[D x 16]          (QK, M=128 N=16)
 //   O^T[D dims x N]      = V^T[D dims x 128 tokens] . P^T[128 x N] (PV, M=128)
 // The query heads of a group are the N dimension of QK (padded to 16).  PV's columns
-// hold each head's probabilities twice, as a rounded part and its remainder (N = 16
-// up to 8 heads, 32 up to 16).  At D = 64, PV still runs with M = 128: its A operand's
-// second 64-row block is given a leading offset of zero, so it reads the same 64
-// dimensions again and TMEM lanes 64-127 hold a copy that nobody stores (cheaper than
-// the M = 64 accumulator layout, and PV is a small part of the tensor pipe's time).
+// hold each head's probabilities twice, as a rounded part and its remainder (16
+// columns up to 8 heads, 32 up to 16).  At D = 64 one PV tile of M = 128 rows covers
+// the chunk's two 64-token halves (see PvGeom), so PV reads each V element once.
+// PV accumulates an item's chunks in tensor memory (one O buffer per item, two
+// buffers); the softmax warps read O once per item.
 //
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
 // head) that work_list_kernel sorts longest first and the CTAs take in snake order;
@@ -34,19 +34,24 @@
 //    rings are separate so that a K stage is reused as soon as its chunk's QK
 //    completes, long before the chunk's V is done with: more of the rings stays in
 //    flight, and the kernel is bound by bytes in flight.
-//  * warp 5, MMA: the whole warp polls (one batched barrier probe per round) and an
-//    elected lane issues PV for the oldest chunk whose probabilities are in shared
-//    memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed; commits
-//    release the ring stages and signal the softmax warps.
+//  * warp 5, MMA: the whole warp polls (one batched probe of five barriers per round)
+//    and an elected lane issues PV for the oldest chunk whose probabilities are in
+//    shared memory, or QK for the next chunk into S[c%2] (TMEM) once its K landed;
+//    commits release the ring stages and the P buffers and signal the softmax warps.
 //  * warps 0-3, and from G = 4 also warps 7-10 (from 16, 7-18), softmax (thread t = TMEM
 //    lane t; a warp reads the lane quarter of its index mod 4, so with eight warps two
-//    share each quarter and take half of the heads each): read S row t (token t, its heads), vote
-//    on whether any score exceeds its head's running max by more than 2^8 (if so,
-//    chunk max across the 128 tokens by a warp reduction + shared memory and an
-//    online-softmax rescale), probabilities split into two parts rounded to the cache
-//    dtype (hi = round(p), lo = round(p - hi)) into P^T (shared memory), then read O
-//    row t (dimension t) of the previous chunk, add its hi and lo columns and
-//    accumulate in registers with the rescale factor.
+//    share each quarter and take half of the heads each): read S row t (token t, its
+//    heads), vote on whether any score exceeds its head's running max by more than 2^8
+//    (if so, chunk max across the 128 tokens by a warp reduction + shared memory and
+//    an online-softmax rescale), probabilities split into two parts rounded to the
+//    cache dtype (hi = round(p), lo = round(p - hi)) into P^T (shared memory).  When
+//    the running max moves after an item's first chunk, the O accumulated so far is
+//    multiplied by the factor before that chunk's PV: the MMA warp, seeing the
+//    chunk's flag, waits for its earlier MMAs to complete and for the softmax warps'
+//    rescale of O in tensor memory (rare: the max moves by more than 2^8).  After an
+//    item's last PV the softmax warps read O row t (dimension t), add its hi and lo
+//    columns and write the output (or the partition's unnormalised O, max and sum),
+//    one chunk later so that the wait overlaps the next item's first chunk.
 //  Rows of the last block past the context end hold real cache data; the softmax
 //  warps zero those V rows in shared memory before PV (a NaN there would survive a
 //  zero weight).
@@ -67,10 +72,32 @@ constexpr int kQHalfBytes = kN * 128;          // 16 query rows x one 64-dimensi
 // P^T holds each probability as two rounded parts, hi = round(p) and
 // lo = round(p - hi), as separate groups of 8 columns: the PV MMA then sums
 // hi + lo in fp32, so rounding p to 16 bits costs about 2^-17 relative instead of
-// 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (N = 16, the columns are there anyway);
-// up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (N = 32).
-constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns
-constexpr uint32_t kTmemCols = 128;            // S[2] at 0/16, O[2] at 32/64 (up to 32 columns each)
+// 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (16 columns, the columns are there anyway);
+// up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (32 columns).
+constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns x 128 tokens
+
+// PV geometry.  At D = 128, PV is O^T[128 dims x NP] = V^T . P^T over the chunk's
+// 128 tokens (8 MMAs of K = 16) and P^T's column groups hold all 128 tokens.  At
+// D = 64 the chunk's two 64-token halves share one M = 128 tile: rows 0-63 of A are
+// dimensions 0-63 of tokens k..k+15 and rows 64-127 the same dimensions of tokens
+// 64+k..64+k+15 (the descriptor's M-block offset is 64 tokens); P^T holds each half
+// in its own column groups (64 tokens each), so N = 2 NP and 4 MMAs cover the chunk.
+// Rows 0-63 x columns [0, NP) then hold the first half's sums, rows 64-127 x
+// [NP, 2 NP) the second's, and the two other blocks cross terms that nobody reads.
+// Without this, a 64-row V^T would be read twice per MMA (twice the shared-memory
+// operand traffic, which is what paces the tensor pipe at these small N).
+template <int D, int GM>
+struct PvGeom {
+  static constexpr bool kHalves = D == 64;
+  static constexpr int kNP = GM <= 8 ? 16 : 32;          // P columns: heads' hi, then lo parts
+  static constexpr int kNO = kHalves ? 2 * kNP : kNP;    // N of PV: O columns per buffer
+  static constexpr int kPTok = kHalves ? 64 : kChunk;    // tokens per P column group
+  static constexpr int kPGroupBytes = kPTok * 16;
+  static constexpr int kSteps = kPTok / 16;              // PV MMAs per chunk
+  // tensor memory: S[2] at 0/16, O[2] at 32 and 32 + kNO
+  static constexpr uint32_t kTmemCols = 32 + 2 * kNO <= 128 ? 128 : 256;
+  static_assert(kNP / 8 * (kHalves ? 2 : 1) * kPGroupBytes <= kPBytes, "P buffer");
+};
 
 // Roles: warps 0-3 softmax, 4 producer of Q and K, 5 MMA, 6 producer of V, and from
 // 4 query heads per KV head warps 7-10 softmax too (from 16, warps 7-18): a warp
@@ -105,11 +132,15 @@ struct TcLayout {
   static constexpr int kOffQ = 2 * kStages * kTileBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  static constexpr int kNumBars = 4 * kStages + 7 * 2 + 1;  // rings (K, V: full, empty), 7 pairs, drain
+  // rings (K, V: full, empty), 8 pairs, rescale handshake (2), drain
+  static constexpr int kNumBars = 4 * kStages + 8 * 2 + 3;
   static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
-  static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;  // [2 chunk slots][4 warps][kN]
-  static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;    // [2 chunk slots][kN]
-  static constexpr int kOffMisc = kOffMTot + 2 * kN * 4;
+  static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;  // [2 item slots][4 warps][kN]
+  static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;    // [2 item slots][kN]
+  static constexpr int kOffAlpha = kOffMTot + 2 * kN * 4;       // [kN] rescale factors
+  // D = 64: the second half's O sums, handed to the threads of the first half's rows
+  static constexpr int kOffXfer = kOffAlpha + kN * 4;           // [64 dims][kN]
+  static constexpr int kOffMisc = kOffXfer + (D == 64 ? 64 * kN * 4 : 0);
   static constexpr int kSmemBytes = kOffMisc + 64;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(kOffQ % 1024 == 0 && kSmemBytes <= 227 * 1024, "layout");
@@ -125,8 +156,11 @@ struct Bars {
   uint64_t* sfull;  // [2] S ready
   uint64_t* sfree;  // [2] S read by the softmax warps
   uint64_t* pfull;  // [2] P written
-  uint64_t* ofull;  // [2] O ready
-  uint64_t* ofree;  // [2] O read
+  uint64_t* pfree;  // [2] the chunk's PV done: P buffer free
+  uint64_t* ofull;  // [2] an item's O complete (its last PV done)
+  uint64_t* ofree;  // [2] an item's O written out
+  uint64_t* cdrain; // every MMA issued before a rescale completed
+  uint64_t* cdone;  // O rescaled by the softmax warps
   uint64_t* drain;  // teardown after an abort
 };
 
@@ -144,9 +178,12 @@ __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
   r.sfull = r.qempty + 2;
   r.sfree = r.sfull + 2;
   r.pfull = r.sfree + 2;
-  r.ofull = r.pfull + 2;
+  r.pfree = r.pfull + 2;
+  r.ofull = r.pfree + 2;
   r.ofree = r.ofull + 2;
-  r.drain = r.ofree + 2;
+  r.cdrain = r.ofree + 2;
+  r.cdone = r.cdrain + 1;
+  r.drain = r.cdone + 1;
   return r;
 }
 
@@ -182,18 +219,24 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   constexpr int kKStages = L::kStages, kVStages = L::kStages;
   constexpr int kGroupBytes = L::kGroupBytes, kTileBytes = L::kTileBytes, kQBytes = L::kQBytes;
   constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
+  using PG = PvGeom<D, GM>;
+  constexpr uint32_t kTmemCols = PG::kTmemCols;
+  constexpr int kNO = PG::kNO;
   extern __shared__ __align__(1024) unsigned char smem[];
   const DecodeParams& p = a.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const Bars bars = carve_bars<D>(smem);
   float* red_max = reinterpret_cast<float*>(smem + L::kOffRedMax);  // [2][4 warps][kN]
-  float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [2 chunk slots][4 warps][kN]
-  float* red_mtot = reinterpret_cast<float*>(smem + L::kOffMTot);   // [2 chunk slots][kN]
+  float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [2 item slots][4 warps][kN]
+  float* red_mtot = reinterpret_cast<float*>(smem + L::kOffMTot);   // [2 item slots][kN]
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kOffAlpha);   // [kN]
+  float* xfer = reinterpret_cast<float*>(smem + L::kOffXfer);       // [64][kN] (D = 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int* kissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 8);   // K chunks issued
   int* vissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 12);  // V chunks issued
   int* qissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 16);  // query tiles issued
+  volatile int* cflag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 20);  // [2] rescale before PV
   const int G = p.group;
 
   if (threadIdx.x == 0) {
@@ -211,9 +254,14 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       mbar_init(&bars.sfull[i], 1);
       mbar_init(&bars.sfree[i], 4 * R::kSplit);
       mbar_init(&bars.pfull[i], 4 * R::kSplit);
+      mbar_init(&bars.pfree[i], 1);
       mbar_init(&bars.ofull[i], 1);
       mbar_init(&bars.ofree[i], 4 * R::kSplit);
+      cflag[i] = 0;
     }
+    mbar_init(bars.cdrain, 1);
+    mbar_init(bars.cdone, 4 * R::kSplit);
+    for (int h = 0; h < kN; ++h) alpha_s[h] = 0.f;  // factors of heads past the group stay 0
     *abort_flag = 0;
     *kissued_slot = 0;
     *vissued_slot = 0;
@@ -338,51 +386,76 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     // The whole warp polls with warp-uniform control flow (descriptors and counters
     // stay in uniform registers) and one elected lane issues whichever is ready: PV of
     // the oldest chunk whose probabilities are written (first: its completion frees a
-    // V stage) or QK of the next chunk (its K landed, its S buffer free).  Neither waits
-    // behind the other.  One round trip probes the four barriers both need.
+    // V stage and a P buffer) or QK of the next chunk (its K landed, its S buffer free).
+    // Neither waits behind the other.  One round trip probes the four barriers both need.
+    // PV accumulates into the item's O buffer (item j: O[j & 1]), overwriting it on the
+    // item's first chunk; the item's last PV also signals O full.
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t idesc_qk = instr_desc_f16(kBf16, false, false, kChunk, kN);
-    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, GM <= 8 ? 16 : 32);
+    constexpr uint32_t idesc_pv = instr_desc_f16(kBf16, true, true, 128, kNO);
     // descriptor bases; adding (byte offset >> 4) moves a descriptor's start address
     const uint64_t dk0 = smem_desc(smem_addr(smem), 16, kGroupBytes, kLayoutSwizzle128);
     const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, 1024, kLayoutSwizzle128);
-    // V^T's second 64-dimension block: 1 KB on at D = 128, the same block again at 64
-    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), D == 128 ? 1024 : 0, kGroupBytes, kLayoutSwizzle128);
-    const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, kChunk * 16, kLayoutNone);
-    // QK cursor: items walked, chunk within the item, chunks in the item
-    ItemCursor qcur;
+    // rows 64-127 of V^T: the second 64-dimension block (1 KB on) at D = 128, the same
+    // dimensions of the tokens 64 on (8 row groups on) at D = 64
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), D == 128 ? 1024 : 8 * kGroupBytes, kGroupBytes,
+                                   kLayoutSwizzle128);
+    const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, PG::kPGroupBytes, kLayoutNone);
+    // QK cursor: items walked, chunk within the item, chunks in the item; PV likewise
+    ItemCursor qcur, pcur;
     qcur.init(p.work_list, num_items);
-    int qk = 0, qj = 0;
+    pcur.init(p.work_list, num_items);
+    int qk = 0, qj = 0, pk = 0, pj = 0;
     int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+    int pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
     int qc = 0, pc = 0;           // next chunk to QK, next chunk to PV
     int qst = 0, qph = 0;         // ring stage and phase of chunk qc
     int pst = 0, pph = 0;         // ring stage and phase of chunk pc
+    int ncorr = 0;                // O rescales handed over so far
     uint64_t idle_since = global_timer_ns();
     while (qcur.valid() || pc < qc) {
       bool progressed = false;
-      const int sb = qc & 1, qb = qj & 1, pb = pc & 1;
-      // bit 0: chunk qc landed, 1: S[qc & 1] free, 2: P of chunk pc written, 3: O[pc & 1] free
+      const int sb = qc & 1, qb = qj & 1, pb = pc & 1, ob = pj & 1;
+      // bit 0: chunk qc landed, 1: S[qc & 1] free, 2: P of chunk pc written, 3: O[pj & 1]
+      // written out (matters on an item's first chunk only), 4: V of chunk pc landed
       const uint32_t seen = __shfl_sync(0xffffffffu,
-          mbar_test_wait4(&bars.kfull[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
-                          (pc >> 1) & 1, &bars.ofree[pb], ((pc >> 1) - 1) & 1), 0);
-      if (pc < qc && (seen & 4) && (pc < 2 || (seen & 8)) &&
-          __all_sync(0xffffffffu, mbar_test_wait(&bars.vfull[pst], pph))) {
+          mbar_test_wait5(&bars.kfull[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
+                          (pc >> 1) & 1, &bars.ofree[ob], ((pj >> 1) - 1) & 1, &bars.vfull[pst], pph), 0);
+      if (pc < qc && (seen & 4) && (pk > 0 || pj < 2 || (seen & 8)) && (seen & 16)) {
+        tc_fence_after();
+        // the running max rose mid-item (rare): O must be rescaled before this PV adds
+        // to it.  Signal when every MMA issued so far has completed, then wait for the
+        // softmax warps to hand the rescaled buffer back.
+        if (cflag[pb]) {
+          if (elect_one()) mma_commit(bars.cdrain);
+          __syncwarp();
+          if (!__all_sync(0xffffffffu, wait_role(bars.cdone, ncorr & 1, abort_flag, p.err, p.wait_limit_ns))) break;
+          ++ncorr;
+          tc_fence_after();
+        }
         const uint64_t dv = dv0 + ((pst * kTileBytes) >> 4);
         const uint64_t dp = dp0 + ((pb * kPBytes) >> 4);
-        tc_fence_after();
+        const bool last = pk == pn - 1;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk)
-            mma_f16(tmem + 32 + pb * 32, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
-                    kk > 0);
-          mma_commit(&bars.ofull[pb]);
+          for (int kk = 0; kk < PG::kSteps; ++kk)
+            mma_f16(tmem + 32 + ob * kNO, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
+                    kk > 0 || pk > 0);
+          mma_commit(&bars.pfree[pb]);
           mma_commit(&bars.vempty[pst]);
+          if (last) mma_commit(&bars.ofull[ob]);
         }
         __syncwarp();
         ++pc;
         if (++pst == kVStages) {
           pst = 0;
           pph ^= 1;
+        }
+        if (++pk == pn) {
+          pk = 0;
+          ++pj;
+          pcur.advance();
+          pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
         }
         progressed = true;
       }
@@ -441,64 +514,82 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const int h0 = warp < 4 ? 0 : ((warp - 7) / 4 + 1) * HG;
     const int t = quarter * 32 + lane;         // TMEM lane: token row of S, dimension row of O (a copy at t >= D)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float m[HG], lp[HG], alpha[HG], alpha_pend[HG], acc[HG];
+    float m[HG], lp[HG], alpha[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
-      m[h] = -INFINITY; lp[h] = 0.f; alpha[h] = 0.f; alpha_pend[h] = 0.f; acc[h] = 0.f;
+      m[h] = -INFINITY; lp[h] = 0.f; alpha[h] = 0.f;
     }
-    // pending chunk (its O not yet consumed): item fields and flags
-    int pend_s = 0, pend_g = 0, pend_part = 0, pend_nparts = 0;
-    bool pend_first = false, pend_last = false, pend_keep = false;
-    int c = 0;
+    // the last finished item, not yet written out (pend_j < 0: none)
+    int pend_s = 0, pend_g = 0, pend_part = 0, pend_nparts = 0, pend_j = -1;
+    int c = 0, j = 0, ncorr = 0;
     bool ok = true;
 
-    // Returns false (warp-uniform) when the wait for O ran out or another role aborted;
-    // the caller then stops at the next collective barrier.
-    auto consume = [&](int cp) -> bool {
-      const int pb = cp & 1;
-      if (!__all_sync(0xffffffffu, wait_role(&bars.ofull[pb], (cp >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)))
-        return false;
-      tc_fence_after();
-      // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16
-      const uint32_t ob = lane_base + 32 + pb * 32 + h0;
-      float o[HG], olo[HG];
-      if (GM <= 8) {  // 4-column aligned loads; a pair at column 2 is picked from them
-        float a4[4], b4[4];
-        tmem_load4x2(ob - (h0 & 3), ob - (h0 & 3) + 8, a4, b4);
+    // Writes out item pend_j once its last PV completed: its O buffer's hi and lo
+    // columns summed, divided by the row sum (a partition instead leaves O unnormalised
+    // with its max and sum for the merge).  Returns false (warp-uniform) when the wait
+    // ran out or another role aborted.
+    auto finalize = [&]() -> bool {
+      const int ob = pend_j & 1;
+      const bool w =
+          __all_sync(0xffffffffu, wait_role(&bars.ofull[ob], (pend_j >> 1) & 1, abort_flag, p.err, p.wait_limit_ns));
+      float o[HG];
+      if (w) {
+        tc_fence_after();
+        // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16; at D = 64
+        // rows 64-127 hold the chunks' second halves in the next NP columns
+        const uint32_t oaddr = lane_base + 32 + ob * kNO + (PG::kHalves && quarter >= 2 ? PG::kNP : 0) + h0;
+        float olo[HG];
+        if (GM <= 8) {  // 4-column aligned loads; a pair at column 2 is picked from them
+          float a4[4], b4[4];
+          tmem_load4x2(oaddr - (h0 & 3), oaddr - (h0 & 3) + 8, a4, b4);
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          o[h] = (h0 & 2) ? a4[(2 + h) & 3] : a4[h];
-          olo[h] = (h0 & 2) ? b4[(2 + h) & 3] : b4[h];
+          for (int h = 0; h < HG; ++h) {
+            o[h] = (h0 & 2) ? a4[(2 + h) & 3] : a4[h];
+            olo[h] = (h0 & 2) ? b4[(2 + h) & 3] : b4[h];
+          }
+        } else if (HG == 4) {
+          tmem_load4x2(oaddr, oaddr + 16, o, olo);
+        } else {
+          tmem_load8x2(oaddr, oaddr + 16, o, olo);
         }
-      } else if (HG == 4) {
-        tmem_load4x2(ob, ob + 16, o, olo);
-      } else {
-        tmem_load8x2(ob, ob + 16, o, olo);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.ofree[pb]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.ofree[ob]);
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        const float v = o[h] + olo[h];  // hi part + lo part
-        acc[h] = pend_first ? v : pend_keep ? acc[h] + v : fmaf(acc[h], alpha_pend[h], v);
+        for (int h = 0; h < HG; ++h) o[h] += olo[h];  // hi part + lo part
       }
-      if (pend_last && t < D) {
-        // the item's totals, left in slot cp & 1 at its last chunk
-        const float* rl = red_l + (cp & 1) * 4 * kN + h0;
+      if (PG::kHalves) {
+        // the second half's sums (rows 64-127) move to the threads of rows 0-63; every
+        // softmax thread takes the barrier, whether its wait succeeded or not
+        if (w && quarter >= 2) {
+#pragma unroll
+          for (int h = 0; h < HG; ++h) xfer[(t - 64) * kN + h0 + h] = o[h];
+        }
+        if (!named_barrier_and(1, NS, w)) return false;
+        if (quarter < 2) {
+#pragma unroll
+          for (int h = 0; h < HG; ++h) o[h] += xfer[t * kN + h0 + h];
+        }
+      } else if (!w) {
+        return false;
+      }
+      if (t < D) {
+        // the item's totals, left in slot ob at its last chunk
+        const float* rl = red_l + ob * 4 * kN + h0;
         const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G + h0;
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           if (h0 + h < G) {
+            const float acc = o[h];
             const float l = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
             const size_t row = row0 + h;
             if (pend_nparts == 1) {
-              store_out<T>(p.out, row * D + t, acc[h] / l, p.out_f32);
+              store_out<T>(p.out, row * D + t, acc / l, p.out_f32);
             } else {
               const size_t k = row * p.max_parts + pend_part;
-              p.ws_o[k * D + t] = acc[h];
+              p.ws_o[k * D + t] = acc;
               if (t == 0) {
-                p.ws_ml[2 * k] = red_mtot[(cp & 1) * kN + h0 + h];
+                p.ws_ml[2 * k] = red_mtot[ob * kN + h0 + h];
                 p.ws_ml[2 * k + 1] = l;
               }
             }
@@ -508,9 +599,42 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       return true;
     };
 
-    bool prev_ok = true;  // outcome of the last consume (warp-uniform)
+    // Rescales the O accumulator of buffer ob by each head's factor before the PV of a
+    // chunk whose scores raised the running max: wait until every MMA issued before
+    // that PV completed, multiply this warp's share of O's columns, hand it back.  All
+    // softmax threads call it (the decision is CTA-uniform).
+    auto rescale = [&](int ob) -> bool {
+      if (quarter == 0 && lane == 0) {
+#pragma unroll
+        for (int h = 0; h < HG; ++h) alpha_s[h0 + h] = h0 + h < G ? alpha[h] : 0.f;
+      }
+      named_barrier_sync(1, NS);
+      if (!__all_sync(0xffffffffu, wait_role(bars.cdrain, ncorr & 1, abort_flag, p.err, p.wait_limit_ns)))
+        return false;
+      ++ncorr;
+      tc_fence_after();
+      // O columns: per half, the heads' hi parts then their lo parts
+      constexpr int kCols = kNO / R::kSplit;   // this warp's share of its lane quarter: 8 to 32
+      const int c0 = (h0 / HG) * kCols;
+      const uint32_t oaddr = lane_base + 32 + ob * kNO + c0;
+#pragma unroll
+      for (int q = 0; q < kCols / 8; ++q) {
+        float v[8];
+        tmem_load8(oaddr + 8 * q, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] *= alpha_s[(c0 + 8 * q + i) % (PG::kNP / 2)];
+        tmem_store8_nowait(oaddr + 8 * q, v);
+      }
+      tmem_store_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.cdone);
+      return true;
+    };
+
+    bool prev_ok = true;  // outcome of the last rescale and write-out (warp-uniform)
     ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
+    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance(), ++j) {
       const Item it = unpack_item(cur.cur, p.part_tokens);
       // padded heads (h >= G) get m = +inf: their scores then come out as -inf and
       // their probabilities as 0 without a test (their l and O are never stored)
@@ -521,7 +645,10 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       }
       for (int k = 0; k < it.nchunks; ++k, ++c) {
         const int sb = c & 1;
-        const bool wok = __all_sync(0xffffffffu, wait_role(&bars.sfull[sb], (c >> 1) & 1, abort_flag, p.err, p.wait_limit_ns));
+        // S of chunk c, and its P buffer free again (the PV of chunk c - 2 completed)
+        const bool wok = __all_sync(0xffffffffu,
+            wait_role2(&bars.sfull[sb], (c >> 1) & 1, c >= 2 ? &bars.pfree[sb] : nullptr, ((c >> 1) - 1) & 1,
+                       abort_flag, p.err, p.wait_limit_ns));
         float sv[HG];
         if (wok) {
           tc_fence_after();
@@ -584,6 +711,10 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
             lp[h] = fmaf(lp[h], alpha[h], pe[h]);
           }
         }
+        // O already holds earlier chunks of this item: it must be rescaled before this
+        // chunk's PV (the MMA warp reads the flag once P is full)
+        const bool corr = !keep && k > 0;
+        if (warp == 0 && lane == 0) cflag[sb] = corr ? 1 : 0;
         // hi = round(p) and lo = round(p - hi) (p - hi is exact in fp32), two heads a
         // word; words past this thread's heads are zero
         uint32_t hw[4], lw[4];
@@ -600,25 +731,28 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         }
         // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns (16
         // bytes) a group: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-7][hi 8-15][lo 0-7][lo
-        // 8-15] for 16
-        unsigned char* pdst = smem + kOffP + sb * kPBytes + (t >> 3) * 128 + (t & 7) * 16;
+        // 8-15] for 16; at D = 64 those groups once per 64-token half
+        const int tt = PG::kHalves ? (t & 63) : t;  // token within its column group
+        unsigned char* pdst = smem + kOffP + sb * kPBytes + (tt >> 3) * 128 + (tt & 7) * 16 +
+                              (PG::kHalves ? (t >> 6) * (PG::kNP / 8) * PG::kPGroupBytes : 0);
+        constexpr int kGB = PG::kPGroupBytes;
         if (R::kSplit == 1) {
           *reinterpret_cast<uint4*>(pdst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(pdst + kChunk * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(pdst + kGB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         } else if (GM == 4) {  // each of the two warps writes its two heads of a group
           *reinterpret_cast<uint32_t*>(pdst + h0 * 2) = hw[0];
-          *reinterpret_cast<uint32_t*>(pdst + kChunk * 16 + h0 * 2) = lw[0];
+          *reinterpret_cast<uint32_t*>(pdst + kGB + h0 * 2) = lw[0];
         } else if (GM == 8) {  // each of the two warps writes its four heads' half of a group
           *reinterpret_cast<uint2*>(pdst + h0 * 2) = make_uint2(hw[0], hw[1]);
-          *reinterpret_cast<uint2*>(pdst + kChunk * 16 + h0 * 2) = make_uint2(lw[0], lw[1]);
+          *reinterpret_cast<uint2*>(pdst + kGB + h0 * 2) = make_uint2(lw[0], lw[1]);
         } else if (HG == 4) {  // 16 heads over four warps: each writes half of a column group
           const int gh = h0 / 8, off = (h0 & 7) * 2;
-          *reinterpret_cast<uint2*>(pdst + gh * kChunk * 16 + off) = make_uint2(hw[0], hw[1]);
-          *reinterpret_cast<uint2*>(pdst + (2 + gh) * kChunk * 16 + off) = make_uint2(lw[0], lw[1]);
+          *reinterpret_cast<uint2*>(pdst + gh * kGB + off) = make_uint2(hw[0], hw[1]);
+          *reinterpret_cast<uint2*>(pdst + (2 + gh) * kGB + off) = make_uint2(lw[0], lw[1]);
         } else {
           const int gh = h0 / 8;  // this warp's column group of hi parts
-          *reinterpret_cast<uint4*>(pdst + gh * kChunk * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(pdst + (2 + gh) * kChunk * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(pdst + gh * kGB) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(pdst + (2 + gh) * kGB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         // rows of the last loaded block past the context end: zero their V rows (only an
         // item's last chunk can have them; the first warp of each quarter does it)
@@ -639,33 +773,36 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.pfull[sb]);
+        prev_ok = true;
+        if (corr) prev_ok = rescale(j & 1);
 
-        if (last) {  // this item's totals (row sums per lane quarter, running max) into slot c & 1
+        if (last) {  // this item's totals (row sums per lane quarter, running max) into slot j & 1
           const float lsum = warp_sum_scatter<HG>(lp, lane);  // head warp_sum_index<HG>(lane)
           if ((lane & (32 / HG - 1)) == 0)
-            red_l[((c & 1) * 4 + quarter) * kN + h0 + warp_sum_index<HG>(lane)] = lsum;
+            red_l[((j & 1) * 4 + quarter) * kN + h0 + warp_sum_index<HG>(lane)] = lsum;
           if (t == 0) {
 #pragma unroll
-            for (int h = 0; h < HG; ++h) red_mtot[(c & 1) * kN + h0 + h] = m[h];
+            for (int h = 0; h < HG; ++h) red_mtot[(j & 1) * kN + h0 + h] = m[h];
           }
-          named_barrier_sync(1, NS);
         }
-        if (c >= 1) prev_ok = consume(c - 1);
-        // chunk c becomes the pending one
-        if (!keep) {
-#pragma unroll
-          for (int h = 0; h < HG; ++h) alpha_pend[h] = alpha[h];
+        // the previous item is written out once this item's first P is on its way (the
+        // vote barrier above made its totals visible)
+        if (k == 0 && pend_j >= 0) {
+          prev_ok = finalize() && prev_ok;
+          pend_j = -1;
         }
-        pend_keep = keep;
-        pend_first = k == 0;
-        pend_last = last;
-        pend_s = it.s;
-        pend_g = it.g;
-        pend_part = it.part;
-        pend_nparts = it.nparts;
+        if (last) {
+          pend_s = it.s;
+          pend_g = it.g;
+          pend_part = it.part;
+          pend_nparts = it.nparts;
+          pend_j = j;
+        }
       }
     }
-    if (ok && prev_ok && c >= 1) consume(c - 1);
+    // the last item: one barrier makes its totals visible (and every thread takes it,
+    // aborted or not)
+    if (named_barrier_and(1, NS, ok && prev_ok) && pend_j >= 0) finalize();
     __syncwarp();
   }
 

@@ -75,6 +75,15 @@ __device__ __forceinline__ bool wait_role(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same for two barriers (b1 may be null): one round trip when both phases have
+// already completed, else one wait after the other.
+__device__ __forceinline__ bool wait_role2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                           volatile int* abort_flag, int* err, uint64_t limit_ns) {
+  if (b1 == nullptr) return wait_role(b0, p0, abort_flag, err, limit_ns);
+  if (mbar_test_wait2(b0, p0, b1, p1) == 3u) return true;
+  return wait_role(b0, p0, abort_flag, err, limit_ns) && wait_role(b1, p1, abort_flag, err, limit_ns);
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <>

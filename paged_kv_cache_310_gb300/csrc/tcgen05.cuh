@@ -160,8 +160,6 @@ __device__ __forceinline__ void tmem_load16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Whole warp: store 16 consecutive 32-bit columns of this thread's TMEM lane, and
-// wait until the stores are done.
 // 32 consecutive columns of this warp's 32 lanes (one row per thread), waited.
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -202,6 +200,17 @@ __device__ __forceinline__ void tmem_store16_words(uint32_t taddr, const uint32_
 }
 __device__ __forceinline__ void tmem_store_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 8 consecutive 32-bit columns of this thread's TMEM lane, NOT waited.
+__device__ __forceinline__ void tmem_store8_nowait(uint32_t taddr, const float* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
+// Whole warp: store 16 consecutive 32-bit columns of this thread's TMEM lane, and
+// wait until the stores are done.
 __device__ __forceinline__ void tmem_store16(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
