@@ -394,6 +394,7 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   p.out = out;
   if (plan.list_bytes > 0) {
     p.work_count = static_cast<int*>(workspace);
+    p.work_next = reinterpret_cast<int*>(static_cast<char*>(workspace) + 128);
     p.work_list = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);
   }
   if (plan.max_parts > 1) {

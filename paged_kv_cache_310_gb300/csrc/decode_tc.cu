@@ -21,10 +21,13 @@
 // buffers); the softmax warps read O once per item.
 //
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
-// head) that work_list_kernel sorts longest first and the CTAs take in snake order;
-// the kernel is launched as a programmatic dependent of that list kernel.  224 threads
+// head) that work_list_kernel sorts longest first; at D = 128 each CTA claims its next
+// item with a global atomic and hands it to its other roles through a shared-memory
+// ring, at D = 64 the CTAs take the items in a fixed snake order (see kClaimItems).
+// The kernel is launched as a programmatic dependent of the list kernel.  224 threads
 // (352 from 4 query heads per KV head, 608 at 16) in five roles:
-//  * warp 4, producer of Q and K: per 128-token chunk, one lane per physical block
+//  * warp 4, producer of Q and K (and, at D = 128, the item claims): per 128-token
+//    chunk, one lane per physical block
 //    reads the block id (before waiting for a free stage, hiding its latency) and
 //    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
 //    128-byte swizzle) into a 96 KB K ring (3 stages at D = 128, 6 at D = 64); blocks
@@ -113,6 +116,23 @@ struct TcRoles {
   static constexpr int kThreads = kSoftmaxThreads + 96;
 };
 
+// Items are not dealt out in a fixed order: the Q/K producer of a CTA claims the next
+// entry of the sorted list with a global atomic when it starts an item, so the longest
+// items go first and whichever CTA gets free takes the next (measured with a fixed
+// snake order: per-CTA chunk counts 113-124 and per-SM speeds within about 5 % left
+// the last CTA 15-22 us behind the first).  The claimed entries reach the other
+// roles through a ring of kItemRing slots in shared memory.
+constexpr int kItemRing = 8;
+// At head_dim 128 claiming measured 3-4 % faster than the fixed snake order on the
+// 7B-like, GQA-70B-like and long-context workloads and 1-2 % on the shared-prefix one.
+// At head_dim 64 it measured slower in every form tried (claims early or late, items
+// read ahead, block ids read ahead, head-major list order: 0.73-0.80 against 0.76-0.83
+// of the copy bandwidth), so the fixed order stays there.
+template <int D>
+constexpr bool kClaimItems = D == 128;
+
+__device__ __forceinline__ bool item_valid(int4 e) { return (e.w & 0xffff) != 0; }  // ntok 0 = end
+
 // Shared-memory layout for head_dim D (64 or 128).  A chunk's K (and V) sits as
 // [8-row group][64-column block][8 rows] of 128-byte rows, 128-byte swizzled: the
 // canonical K-major layout for the QK A operand (8-row groups kGroupBytes apart,
@@ -132,8 +152,8 @@ struct TcLayout {
   static constexpr int kOffQ = 2 * kStages * kTileBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
-  // rings (K, V: full, empty), 8 pairs, rescale handshake (2), drain
-  static constexpr int kNumBars = 4 * kStages + 8 * 2 + 3;
+  // rings (K, V: full, empty), 8 pairs, rescale handshake (2), drain, item ring
+  static constexpr int kNumBars = 4 * kStages + 8 * 2 + 3 + 2 * kItemRing;
   static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;  // [2 item slots][4 warps][kN]
   static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;    // [2 item slots][kN]
@@ -141,7 +161,8 @@ struct TcLayout {
   // D = 64: the second half's O sums, handed to the threads of the first half's rows
   static constexpr int kOffXfer = kOffAlpha + kN * 4;           // [64 dims][kN]
   static constexpr int kOffMisc = kOffXfer + (D == 64 ? 64 * kN * 4 : 0);
-  static constexpr int kSmemBytes = kOffMisc + 64;
+  static constexpr int kOffRing = (kOffMisc + 64 + 15) / 16 * 16;  // [kItemRing] work-list entries
+  static constexpr int kSmemBytes = kOffRing + kItemRing * 16;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(kOffQ % 1024 == 0 && kSmemBytes <= 227 * 1024, "layout");
 };
@@ -162,6 +183,8 @@ struct Bars {
   uint64_t* cdrain; // every MMA issued before a rescale completed
   uint64_t* cdone;  // O rescaled by the softmax warps
   uint64_t* drain;  // teardown after an abort
+  uint64_t* ifull;  // [kItemRing] slot written by the producer
+  uint64_t* iempty; // [kItemRing] slot read by every other role
 };
 
 template <int D>
@@ -184,6 +207,8 @@ __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
   r.cdrain = r.ofree + 2;
   r.cdone = r.cdrain + 1;
   r.drain = r.cdone + 1;
+  r.ifull = r.drain + 1;
+  r.iempty = r.ifull + kItemRing;
   return r;
 }
 
@@ -221,6 +246,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
   using PG = PvGeom<D, GM>;
   constexpr uint32_t kTmemCols = PG::kTmemCols;
+  constexpr bool kDyn = kClaimItems<D>;
   constexpr int kNO = PG::kNO;
   extern __shared__ __align__(1024) unsigned char smem[];
   const DecodeParams& p = a.p;
@@ -237,6 +263,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   int* vissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 12);  // V chunks issued
   int* qissued_slot = reinterpret_cast<int*>(smem + L::kOffMisc + 16);  // query tiles issued
   volatile int* cflag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 20);  // [2] rescale before PV
+  int4* ring = reinterpret_cast<int4*>(smem + L::kOffRing);
   const int G = p.group;
 
   if (threadIdx.x == 0) {
@@ -262,6 +289,10 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     mbar_init(bars.cdrain, 1);
     mbar_init(bars.cdone, 4 * R::kSplit);
     for (int h = 0; h < kN; ++h) alpha_s[h] = 0.f;  // factors of heads past the group stay 0
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bars.ifull[i], 1);
+      mbar_init(&bars.iempty[i], 2 + 4 * R::kSplit);  // V producer, MMA warp, softmax warps
+    }
     *abort_flag = 0;
     *kissued_slot = 0;
     *vissued_slot = 0;
@@ -298,9 +329,46 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row outside the pool
     int c = 0, j = 0;
     bool ok = true;
-    ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
-      const Item it = unpack_item(cur.cur, p.part_tokens);
+    // Claiming (D = 128): item j + 1's list index is claimed four chunks before item j's
+    // last chunk is issued (about when this CTA's rings run out of item j), its entry
+    // read two chunks before, and it is published in the ring with that last chunk, so
+    // neither latency stalls the issue.  Claiming that late keeps the CTAs that run at
+    // the same time on neighbouring entries of the list: the shared-prefix workload's
+    // L2 reuse depends on it (claims at the start of each item measured 0.95 there
+    // against 1.01-1.02).  Lane 0 does all of it.
+    auto publish = [&](int jj, int4 e) -> bool {
+      const int r = jj % kItemRing;
+      if (jj >= kItemRing &&
+          !wait_role(&bars.iempty[r], ((jj / kItemRing) - 1) & 1, abort_flag, p.err, p.wait_limit_ns))
+        return false;
+      ring[r] = e;
+      mbar_arrive(&bars.ifull[r]);
+      return true;
+    };
+    int idx = 0;                        // lane 0: list index of the next item
+    int4 e = make_int4(0, 0, 0, 0);     // claimed: the current item (then the next one, lane 0)
+    ItemCursor sc;                      // fixed order (no claiming): this CTA's items
+    if constexpr (!kDyn) {
+      sc.init(p.work_list, num_items);
+    } else if (lane == 0) {
+      idx = atomicAdd(p.work_next, 1);
+      if (idx < num_items) e = p.work_list[idx];
+      ok = publish(0, e);
+    }
+    for (;; ++j) {
+      if constexpr (!kDyn) {
+        if (!(sc.valid() && ok)) break;
+        e = sc.cur;
+      } else {
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        e.x = __shfl_sync(0xffffffffu, e.x, 0);
+        e.y = __shfl_sync(0xffffffffu, e.y, 0);
+        e.z = __shfl_sync(0xffffffffu, e.z, 0);
+        e.w = __shfl_sync(0xffffffffu, e.w, 0);
+        if (!ok || !item_valid(e)) break;
+      }
+      const Item it = unpack_item(e, p.part_tokens);
+      int4 nxt = make_int4(0, 0, 0, 0);  // lane 0: the entry of item j + 1
       const int qb = j & 1;
       if (lane == 0) {
         ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
@@ -340,9 +408,17 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           }
           tma_load_4d(smem + st * kTileBytes + lane * bs * (D * 2), &a.tk, row / 8, &bars.kfull[st], pol_stream);
         }
-        if (lane == 0) *kissued_slot = c + 1;
+        if (lane == 0) {
+          *kissued_slot = c + 1;
+          if constexpr (kDyn) {
+            if (k == max(0, it.nchunks - 4)) idx = atomicAdd(p.work_next, 1);
+            if (k == max(0, it.nchunks - 2)) nxt = idx < num_items ? p.work_list[idx] : make_int4(0, 0, 0, 0);
+            if (k == it.nchunks - 1) ok = publish(j + 1, nxt);
+          }
+        }
       }
-      ++j;
+      if constexpr (kDyn) e = nxt;  // lane 0's copy is the one broadcast
+      else sc.advance();
     }
   } else if (warp == 6) {
     // ============================ TMA producer of V ============================
@@ -353,9 +429,24 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const int oob_row = p.num_blocks * p.num_kv_heads * bs;
     int c = 0;
     bool ok = true;
-    ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance()) {
-      const Item it = unpack_item(cur.cur, p.part_tokens);
+    ItemCursor vcur;  // fixed order (no claiming)
+    if constexpr (!kDyn) vcur.init(p.work_list, num_items);
+    for (int j = 0;; ++j) {
+      int4 e = make_int4(0, 0, 0, 0);
+      if constexpr (!kDyn) {
+        if (!(vcur.valid() && ok)) break;
+        e = vcur.cur;
+      } else {
+        if (!ok) break;
+        const int r = j % kItemRing;
+        ok = __all_sync(0xffffffffu, wait_role(&bars.ifull[r], (j / kItemRing) & 1, abort_flag, p.err, p.wait_limit_ns));
+        if (!ok) break;
+        e = ring[r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.iempty[r]);
+        if (!item_valid(e)) break;
+      }
+      const Item it = unpack_item(e, p.part_tokens);
       const int32_t* table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks_per_seq;
       for (int k = 0; k < it.nchunks && ok; ++k, ++c) {
         const int st = c % kVStages;
@@ -380,6 +471,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         }
         if (lane == 0) *vissued_slot = c + 1;
       }
+      if constexpr (!kDyn) vcur.advance();
     }
   } else if (warp == 5) {
     // ============================ MMA issuer ============================
@@ -401,20 +493,36 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), D == 128 ? 1024 : 8 * kGroupBytes, kGroupBytes,
                                    kLayoutSwizzle128);
     const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, PG::kPGroupBytes, kLayoutNone);
-    // QK cursor: items walked, chunk within the item, chunks in the item; PV likewise
-    ItemCursor qcur, pcur;
-    qcur.init(p.work_list, num_items);
-    pcur.init(p.work_list, num_items);
-    int qk = 0, qj = 0, pk = 0, pj = 0;
-    int qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
-    int pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
+    // QK cursor: items walked, chunk within the item, chunks in the item (0: the item
+    // is not read from the ring yet); PV likewise.  QK reads an item's ring slot first
+    // (as soon as it is published); PV reads the same slot when it starts the item and
+    // then releases it.
+    int qk = 0, qj = 0, pk = 0, pj = 0, qn = 0, pn = 0;
+    bool qdone = false;  // QK read the end of the list
+    ItemCursor qcur, pcur;  // fixed order (no claiming): each item's count is known at once
+    if constexpr (!kDyn) {
+      qcur.init(p.work_list, num_items);
+      pcur.init(p.work_list, num_items);
+      qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+      pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
+      qdone = !qcur.valid();
+    }
     int qc = 0, pc = 0;           // next chunk to QK, next chunk to PV
     int qst = 0, qph = 0;         // ring stage and phase of chunk qc
     int pst = 0, pph = 0;         // ring stage and phase of chunk pc
     int ncorr = 0;                // O rescales handed over so far
     uint64_t idle_since = global_timer_ns();
-    while (qcur.valid() || pc < qc) {
+    while (!qdone || pc < qc) {
       bool progressed = false;
+      if constexpr (kDyn) {
+        if (qn == 0 && !qdone &&
+            __all_sync(0xffffffffu, mbar_test_wait(&bars.ifull[qj % kItemRing], (qj / kItemRing) & 1))) {
+          const int4 e = ring[qj % kItemRing];
+          if (item_valid(e)) qn = unpack_item(e, p.part_tokens).nchunks;
+          else qdone = true;
+          progressed = true;
+        }
+      }
       const int sb = qc & 1, qb = qj & 1, pb = pc & 1, ob = pj & 1;
       // bit 0: chunk qc landed, 1: S[qc & 1] free, 2: P of chunk pc written, 3: O[pj & 1]
       // written out (matters on an item's first chunk only), 4: V of chunk pc landed
@@ -422,6 +530,13 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           mbar_test_wait5(&bars.kfull[qst], qph, &bars.sfree[sb], ((qc >> 1) - 1) & 1, &bars.pfull[pb],
                           (pc >> 1) & 1, &bars.ofree[ob], ((pj >> 1) - 1) & 1, &bars.vfull[pst], pph), 0);
       if (pc < qc && (seen & 4) && (pk > 0 || pj < 2 || (seen & 8)) && (seen & 16)) {
+        if constexpr (kDyn) {
+          if (pk == 0) {  // PV starts item pj: its chunk count, then the slot is free
+            pn = unpack_item(ring[pj % kItemRing], p.part_tokens).nchunks;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.iempty[pj % kItemRing]);
+          }
+        }
         tc_fence_after();
         // the running max rose mid-item (rare): O must be rescaled before this PV adds
         // to it.  Signal when every MMA issued so far has completed, then wait for the
@@ -454,12 +569,14 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (++pk == pn) {
           pk = 0;
           ++pj;
-          pcur.advance();
-          pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
+          if constexpr (!kDyn) {
+            pcur.advance();
+            pn = pcur.valid() ? unpack_item(pcur.cur, p.part_tokens).nchunks : 0;
+          }
         }
         progressed = true;
       }
-      if (qcur.valid() && (seen & 1) && (qc < 2 || (seen & 2)) &&
+      if (qn > 0 && (seen & 1) && (qc < 2 || (seen & 2)) &&
           (qk > 0 || __all_sync(0xffffffffu, mbar_test_wait(&bars.qfull[qb], (qj >> 1) & 1)))) {
         const uint64_t dk = dk0 + ((qst * kTileBytes) >> 4);
         const uint64_t dq = dq0 + ((qb * kQBytes) >> 4);
@@ -485,8 +602,13 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (++qk == qn) {
           qk = 0;
           ++qj;
-          qcur.advance();
-          qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+          if constexpr (kDyn) {
+            qn = 0;
+          } else {
+            qcur.advance();
+            qn = qcur.valid() ? unpack_item(qcur.cur, p.part_tokens).nchunks : 0;
+            qdone = !qcur.valid();
+          }
         }
         progressed = true;
       }
@@ -633,9 +755,30 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     };
 
     bool prev_ok = true;  // outcome of the last rescale and write-out (warp-uniform)
-    ItemCursor cur;
-    for (cur.init(p.work_list, num_items); cur.valid() && ok; cur.advance(), ++j) {
-      const Item it = unpack_item(cur.cur, p.part_tokens);
+    ItemCursor scur;  // fixed order (no claiming)
+    if constexpr (!kDyn) scur.init(p.work_list, num_items);
+    for (;; ++j) {
+      int4 e = make_int4(0, 0, 0, 0);
+      if constexpr (!kDyn) {
+        if (!(scur.valid() && ok)) break;
+        e = scur.cur;
+      } else {
+        if (!ok) break;
+        const int r = j % kItemRing;
+        const bool w =
+            __all_sync(0xffffffffu, wait_role(&bars.ifull[r], (j / kItemRing) & 1, abort_flag, p.err, p.wait_limit_ns));
+        if (w) e = ring[r];
+        __syncwarp();
+        if (lane == 0 && w) mbar_arrive(&bars.iempty[r]);
+        // every softmax thread takes this barrier: after an abort some warps may have
+        // given up on the slot while others read it, and all must leave together
+        if (!named_barrier_and(1, NS, w)) {
+          prev_ok = false;
+          break;
+        }
+        if (!item_valid(e)) break;
+      }
+      const Item it = unpack_item(e, p.part_tokens);
       // padded heads (h >= G) get m = +inf: their scores then come out as -inf and
       // their probabilities as 0 without a test (their l and O are never stored)
 #pragma unroll
@@ -799,6 +942,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           pend_j = j;
         }
       }
+      if constexpr (!kDyn) scur.advance();
     }
     // the last item: one barrier makes its totals visible (and every thread takes it,
     // aborted or not)
@@ -854,6 +998,7 @@ constexpr int kMaxChunkCounts = kTcMaxPartition / kChunk;
 template <typename T>
 __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_constant__ DecodeParams p) {
   grid_dependents_launch();  // the decode kernel may start its prologue now
+  if (threadIdx.x == 0) *p.work_next = 0;  // the decode CTAs claim items from 0 on
   __shared__ int hist[kMaxChunkCounts + 1];
   __shared__ int next[kMaxChunkCounts + 1];
   const int full_chunks = p.part_tokens / kChunk;
