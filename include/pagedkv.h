@@ -59,8 +59,10 @@
  *    either that dtype or f32; head_dim 64 or 128; block_size 8, 16, 32 or 64;
  *    num_q_heads a multiple of num_kv_heads.  Group size (query heads per KV head)
  *    up to 8 on the CUDA-core decode path; on the tensor-core decode path up to 16
- *    for f16/bf16 and up to 8 for f32 (tf32 MMAs on split operands, within the f32
- *    tolerance); prefill on tensor cores for f16/bf16, groups up to 16.
+ *    for f16/bf16 and up to 8 for f32 (tf32 MMAs on split operands: scores to about
+ *    2^-21 relative, within the f32 tolerance for logits of a few units; for logits
+ *    of tens of units choose PKV_PATH_CUDA_CORE, fp32 throughout); prefill on tensor
+ *    cores for f16/bf16, groups up to 16.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
