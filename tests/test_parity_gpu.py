@@ -306,6 +306,24 @@ def test_head_dim_64_empty_single_and_split(path):
                 assert same_bytes(got[s_, h], vc[b, h // 8, 0])
 
 
+@pytest.mark.parametrize("head_dim", [128, 64], ids=["claimed_items", "fixed_order"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
+def test_all_contexts_empty(path, head_dim):
+    """No sequence has a token: the work list is empty, so every CTA of the tensor-core
+    kernel finds the end of the list at once (by claim at head_dim 128, in the fixed
+    order at 64), and every output row is zero."""
+    ctx = [0] * 5
+    keys, owned = workloads.private_layout(ctx, 16)
+    w = workloads.build_from_layout(name="all empty", seed=310_471, dtype="bf16", num_q_heads=16,
+                                    num_kv_heads=4, head_dim=head_dim, block_size=16, ctx=ctx, block_keys=keys,
+                                    owned_rows=owned, cow=[], num_blocks=3, canary=True,
+                                    gen=torch.Generator().manual_seed(310_471))
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=path)
+    assert (out.cpu() == 0).all()
+    check_close(out, ref, w.dtype)
+
+
 # ------------------------------------------------------------------------------------
 # invariants on the GPU
 
