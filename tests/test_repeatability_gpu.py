@@ -2,7 +2,10 @@
 deterministic, and a race in their pipelines (a stage reused too early, a buffer read
 before it landed) would show up as a differing repeat.  Decode runs on the GQA-70B-like
 batch (tensor cores, dependent launches after the append) and with split-K partitions
-on both paths at both head sizes; prefill on a chunked-prefill batch."""
+on both paths at both head sizes; prefill on a chunked-prefill batch.  At head_dim 128
+the tensor-core CTAs claim their items as they get free, so which CTA computes an item
+changes from call to call: equal bits also show that the result does not depend on
+where an item runs."""
 import pytest
 import torch
 
