@@ -116,8 +116,8 @@ struct TcRoles {
   static constexpr int kThreads = kSoftmaxThreads + 96;
 };
 
-// Items are not dealt out in a fixed order: the Q/K producer of a CTA claims the next
-// entry of the sorted list with a global atomic when it starts an item, so the longest
+// Claimed items (head_dim 128): the Q/K producer of a CTA takes the next entry of the
+// sorted list with a global atomic as it runs out of its current item, so the longest
 // items go first and whichever CTA gets free takes the next (measured with a fixed
 // snake order: per-CTA chunk counts 113-124 and per-SM speeds within about 5 % left
 // the last CTA 15-22 us behind the first).  The claimed entries reach the other
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     // stay in uniform registers) and one elected lane issues whichever is ready: PV of
     // the oldest chunk whose probabilities are written (first: its completion frees a
     // V stage and a P buffer) or QK of the next chunk (its K landed, its S buffer free).
-    // Neither waits behind the other.  One round trip probes the four barriers both need.
+    // Neither waits behind the other.  One round trip probes the five barriers both need.
     // PV accumulates into the item's O buffer (item j: O[j & 1]), overwriting it on the
     // item's first chunk; the item's last PV also signals O full.
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
