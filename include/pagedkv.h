@@ -186,7 +186,9 @@ pkv_status paged_block_swap_in(const int64_t* block_ids, int32_t num_ids, const 
  * Bytes of workspace paged_attention_decode needs for these sizes and config.  The
  * CUDA-core path needs none when every sequence fits one partition; the tensor-core
  * path always needs room for its work list (16 bytes per (sequence, KV head,
- * partition) plus 256) and, past one partition, the partition partials.
+ * partition) plus a 256-byte header holding the entry count and the counter from
+ * which the CTAs claim entries) and, past one partition, the partition partials.
+ * Two calls in flight at once (on different streams) need separate workspaces.
  * max_context_len: host upper bound on context_lens.  Returns 0 for invalid
  * arguments as well (then the decode call itself reports the error).
  */
