@@ -181,14 +181,14 @@ def test_scales_other_than_inverse_sqrt_d(scale, path):
     check_rounded(low, out)
 
 
-def rising_scores_workload(dtype):
+def rising_scores_workload(dtype, head_dim=128, num_q_heads=16, num_kv_heads=2):
     """Scores that rise by about 11 (log2 units) from one 128-token chunk to the next
     for every head: each KV head g has a unit direction u_g, its query heads are
     sqrt(D) u_g plus noise, and key j gets 8 * (j // 128) u_g added.  Every head's
     running max then moves on every chunk."""
     import dataclasses
-    w = workloads.random_workload(310_477, num_seqs=5, max_len=1500, min_len=700, num_q_heads=16, num_kv_heads=2,
-                                  head_dim=128, block_size=16, dtype=dtype)
+    w = workloads.random_workload(310_477, num_seqs=5, max_len=1500, min_len=700, num_q_heads=num_q_heads,
+                                  num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=16, dtype=dtype)
     S, Hq, D = w.q.shape
     Hkv, bs, G = w.num_kv_heads, w.block_size, w.num_q_heads // w.num_kv_heads
     gen = torch.Generator().manual_seed(477)
@@ -322,6 +322,21 @@ def test_all_contexts_empty(path, head_dim):
     out, g = gpu_step(w, torch.float32, path=path)
     assert (out.cpu() == 0).all()
     check_close(out, ref, w.dtype)
+
+
+@pytest.mark.parametrize("group", [1, 8, 16])
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_running_max_rising_tensor_core_shapes(head_dim, group):
+    """The rescale of O in tensor memory at both head sizes and at 1, 8 and 16 query
+    heads per KV head: the head_dim-64 O buffer holds the two 64-token halves in
+    separate columns, and the columns each softmax warp rescales depend on the group."""
+    w = rising_scores_workload("bf16", head_dim=head_dim, num_q_heads=2 * group, num_kv_heads=2)
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=pkv.PATH_TENSOR_CORE)
+    check_close(out, ref, w.dtype)
+    low = decode_only(w, g, w.dtype, path=pkv.PATH_TENSOR_CORE)
+    check_in_dtype(low, ref)
+    check_rounded(low, out)
 
 
 # ------------------------------------------------------------------------------------
