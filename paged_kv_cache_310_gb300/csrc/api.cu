@@ -413,6 +413,7 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
   p.head_dim = cache->head_dim;
   p.part_tokens = plan.part_tokens;
   p.max_parts = plan.max_parts;
+  p.heads_per_item = 1;  // the tensor-core launcher pairs heads where it can
   p.out_f32 = out_dtype == PKV_F32 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
   p.wait_limit_ns = g_wait_limit_ns.load();

@@ -21,9 +21,11 @@
 // buffers); the softmax warps read O once per item.
 //
 // Persistent CTAs (one per SM) over a work list of items = (partition, sequence, KV
-// head) that work_list_kernel sorts longest first; at D = 128 each CTA claims its next
-// item with a global atomic and hands it to its other roles through a shared-memory
-// ring, at D = 64 the CTAs take the items in a fixed snake order (see kClaimItems).
+// head, or at D = 64 a pair of KV heads where they pair up: see kPair) that
+// work_list_kernel sorts longest first; with head_dim-128 operands each CTA claims its
+// next item with a global atomic and hands it to its other roles through a
+// shared-memory ring, at D = 64 unpaired the CTAs take the items in a fixed snake
+// order (see kClaimItems).
 // The kernel is launched as a programmatic dependent of the list kernel.  224 threads
 // (352 from 4 query heads per KV head, 608 at 16) in five roles:
 //  * warp 4, producer of Q and K (and, at D = 128, the item claims): per 128-token
@@ -131,6 +133,19 @@ constexpr int kItemRing = 8;
 template <int D>
 constexpr bool kClaimItems = D == 128;
 
+// Paired heads (head_dim 64, an even number of KV heads, up to 8 query heads per KV
+// head): a work item covers KV heads 2i and 2i + 1.  In the pool their tiles of a block
+// are adjacent, so one TMA box lands row r of both as one 256-byte operand row (head
+// 2i's 64 dimensions as column block 0, head 2i + 1's as block 1), the head_dim-128
+// shared-memory layout, and the item runs the head_dim-128 pipeline: 32 KB chunks and
+// the 16-column geometry.  QK's query operand is block diagonal: columns 0-7 hold the
+// first head's query rows in dimension block 0 (zeros in block 1), columns 8-15 the
+// second head's in block 1, so each S column sees its own head's K only.  PV computes
+// O^T = V^T . P^T over all 128 rows; rows 0-63 (the first head's dimensions) are read
+// in columns 0-7 and rows 64-127 in columns 8-15, the other two blocks are cross terms
+// nobody reads.  With 16 KB chunks of one head the per-chunk costs (barrier round
+// trips, the softmax pass, item changes) weigh twice as much per byte.
+
 __device__ __forceinline__ bool item_valid(int4 e) { return (e.w & 0xffff) != 0; }  // ntok 0 = end
 
 // Shared-memory layout for head_dim D (64 or 128).  A chunk's K (and V) sits as
@@ -237,21 +252,25 @@ __device__ __forceinline__ Item unpack_item(int4 e, int part_tokens) {
   return it;
 }
 
-template <typename T, int D, int GM>
+// kPair (head_dim D = 64, up to 8 query heads per KV head): an item covers two
+// adjacent KV heads and runs with head_dim-128 operands (see the paired-heads note above).
+template <typename T, int D, int GM, bool kPair>
 __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
-  using L = TcLayout<D>;
+  static_assert(!kPair || (D == 64 && GM == 16), "paired heads: head_dim 64, the 16-column geometry");
+  constexpr int DL = kPair ? 128 : D;  // operand width: dimensions of a K/V row in shared memory
+  using L = TcLayout<DL>;
   using R = TcRoles<GM>;
   constexpr int kKStages = L::kStages, kVStages = L::kStages;
   constexpr int kGroupBytes = L::kGroupBytes, kTileBytes = L::kTileBytes, kQBytes = L::kQBytes;
   constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
-  using PG = PvGeom<D, GM>;
+  using PG = PvGeom<DL, GM>;
   constexpr uint32_t kTmemCols = PG::kTmemCols;
-  constexpr bool kDyn = kClaimItems<D>;
+  constexpr bool kDyn = kClaimItems<DL>;
   constexpr int kNO = PG::kNO;
   extern __shared__ __align__(1024) unsigned char smem[];
   const DecodeParams& p = a.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Bars bars = carve_bars<D>(smem);
+  const Bars bars = carve_bars<DL>(smem);
   float* red_max = reinterpret_cast<float*>(smem + L::kOffRedMax);  // [2][4 warps][kN]
   float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [2 item slots][4 warps][kN]
   float* red_mtot = reinterpret_cast<float*>(smem + L::kOffMTot);   // [2 item slots][kN]
@@ -265,6 +284,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   volatile int* cflag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 20);  // [2] rescale before PV
   int4* ring = reinterpret_cast<int4*>(smem + L::kOffRing);
   const int G = p.group;
+  // S/O column n holds a query head of the item: n < G; paired, n % 8 < G (the first
+  // head's group in columns 0-7, the second's in 8-15)
+  auto col_ok = [G](int n) { return kPair ? (n & 7) < G : n < G; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -304,6 +326,12 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   // a group of 8 columns) must read as zero
   for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += R::kThreads)
     reinterpret_cast<uint4*>(smem + kOffP)[i] = make_uint4(0, 0, 0, 0);
+  // paired heads: the query operand's off-diagonal blocks (the first head's rows in the
+  // second head's dimensions and back) are never loaded and must read as zero
+  if constexpr (kPair) {
+    for (int i = threadIdx.x; i < 2 * kQBytes / 16; i += R::kThreads)
+      reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -329,13 +357,13 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row outside the pool
     int c = 0, j = 0;
     bool ok = true;
-    // Claiming (D = 128): item j + 1's list index is claimed four chunks before item j's
-    // last chunk is issued (about when this CTA's rings run out of item j), its entry
-    // read two chunks before, and it is published in the ring with that last chunk, so
-    // neither latency stalls the issue.  Claiming that late keeps the CTAs that run at
-    // the same time on neighbouring entries of the list: the shared-prefix workload's
-    // L2 reuse depends on it (claims at the start of each item measured 0.95 there
-    // against 1.01-1.02).  Lane 0 does all of it.
+    // Claiming (head_dim-128 operands): item j + 1's list index is claimed four chunks
+    // before item j's last chunk is issued (about when this CTA's rings run out of item
+    // j), its entry read two chunks before, and it is published in the ring with that
+    // last chunk, so neither latency stalls the issue.  Claiming that late keeps the
+    // CTAs that run at the same time on neighbouring entries of the list: the
+    // shared-prefix workload's L2 reuse depends on it (claims at the start of each item
+    // measured 0.95 there against 1.01-1.02).  Lane 0 does all of it.
     auto publish = [&](int jj, int4 e) -> bool {
       const int r = jj % kItemRing;
       if (jj >= kItemRing &&
@@ -373,12 +401,21 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       if (lane == 0) {
         ok = j < 2 || wait_role(&bars.qempty[qb], ((j >> 1) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
         if (ok) {
-          mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
           unsigned char* qdst = smem + kOffQ + qb * kQBytes;
-          const int qrow = it.s * p.num_q_heads + it.g * G;
+          if constexpr (kPair) {
+            // 8 query rows from the first head's group into rows 0-7 of dimension block
+            // 0, 8 from the second's into rows 8-15 of block 1 (box 64 x 8)
+            const int qrow = it.s * p.num_q_heads + it.g * 2 * G;
+            mbar_arrive_expect_tx(&bars.qfull[qb], 2 * 8 * 128);
+            tma_load_2d(qdst, &a.tq, 0, qrow, &bars.qfull[qb], pol_keep);
+            tma_load_2d(qdst + kQHalfBytes + 8 * 128, &a.tq, 0, qrow + G, &bars.qfull[qb], pol_keep);
+          } else {
+            const int qrow = it.s * p.num_q_heads + it.g * G;
+            mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
 #pragma unroll
-          for (int cb = 0; cb < L::kBlocks; ++cb)
-            tma_load_2d(qdst + cb * kQHalfBytes, &a.tq, 64 * cb, qrow, &bars.qfull[qb], pol_keep);
+            for (int cb = 0; cb < L::kBlocks; ++cb)
+              tma_load_2d(qdst + cb * kQHalfBytes, &a.tq, 64 * cb, qrow, &bars.qfull[qb], pol_keep);
+          }
           *qissued_slot = j + 1;
         }
       }
@@ -404,9 +441,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
               set_error(p.err, kErrIndex);
               b = 0;
             }
-            row = (b * p.num_kv_heads + it.g) * bs;
+            row = (b * p.num_kv_heads + it.g * p.heads_per_item) * bs;
           }
-          tma_load_4d(smem + st * kTileBytes + lane * bs * (D * 2), &a.tk, row / 8, &bars.kfull[st], pol_stream);
+          tma_load_4d(smem + st * kTileBytes + lane * bs * (DL * 2), &a.tk, row / 8, &bars.kfull[st], pol_stream);
         }
         if (lane == 0) {
           *kissued_slot = c + 1;
@@ -464,9 +501,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           int row = oob_row;
           if (live) {
             if (b < 0 || b >= p.num_blocks) b = 0;  // the K producer flags it
-            row = (b * p.num_kv_heads + it.g) * bs;
+            row = (b * p.num_kv_heads + it.g * p.heads_per_item) * bs;
           }
-          tma_load_4d(smem + kOffV + st * kTileBytes + lane * bs * (D * 2), &a.tv, row / 8, &bars.vfull[st],
+          tma_load_4d(smem + kOffV + st * kTileBytes + lane * bs * (DL * 2), &a.tv, row / 8, &bars.vfull[st],
                       pol_stream);
         }
         if (lane == 0) *vissued_slot = c + 1;
@@ -490,7 +527,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     const uint64_t dq0 = smem_desc(smem_addr(smem + kOffQ), 16, 1024, kLayoutSwizzle128);
     // rows 64-127 of V^T: the second 64-dimension block (1 KB on) at D = 128, the same
     // dimensions of the tokens 64 on (8 row groups on) at D = 64
-    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), D == 128 ? 1024 : 8 * kGroupBytes, kGroupBytes,
+    const uint64_t dv0 = smem_desc(smem_addr(smem + kOffV), DL == 128 ? 1024 : 8 * kGroupBytes, kGroupBytes,
                                    kLayoutSwizzle128);
     const uint64_t dp0 = smem_desc(smem_addr(smem + kOffP), 128, PG::kPGroupBytes, kLayoutNone);
     // QK cursor: items walked, chunk within the item, chunks in the item (0: the item
@@ -584,7 +621,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         tc_fence_after();
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < DL / 16; ++kk) {
             const uint32_t ko = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
             const uint32_t qo = ((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4;
             mma_f16(tmem + sb * 16, dk + ko, dq + qo, idesc_qk, kk > 0);
@@ -695,22 +732,26 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       } else if (!w) {
         return false;
       }
-      if (t < D) {
+      // paired: rows 0-63 are the first head's dimensions, rows 64-127 the second's;
+      // a thread writes the columns of its own head only
+      if (kPair || t < D) {
+        const int dim = kPair ? (t & 63) : t;
         // the item's totals, left in slot ob at its last chunk
         const float* rl = red_l + ob * 4 * kN + h0;
-        const size_t row0 = static_cast<size_t>(pend_s) * p.num_q_heads + pend_g * G + h0;
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-          if (h0 + h < G) {
+          const int n = h0 + h;
+          if (col_ok(n) && (!kPair || (n >> 3) == (t >> 6))) {
             const float acc = o[h];
             const float l = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
-            const size_t row = row0 + h;
+            const size_t row = static_cast<size_t>(pend_s) * p.num_q_heads +
+                               (kPair ? pend_g * 2 * G + (n >> 3) * G + (n & 7) : pend_g * G + n);
             if (pend_nparts == 1) {
-              store_out<T>(p.out, row * D + t, acc / l, p.out_f32);
+              store_out<T>(p.out, row * D + dim, acc / l, p.out_f32);
             } else {
               const size_t k = row * p.max_parts + pend_part;
-              p.ws_o[k * D + t] = acc;
-              if (t == 0) {
+              p.ws_o[k * D + dim] = acc;
+              if (dim == 0) {
                 p.ws_ml[2 * k] = red_mtot[ob * kN + h0 + h];
                 p.ws_ml[2 * k + 1] = l;
               }
@@ -728,7 +769,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     auto rescale = [&](int ob) -> bool {
       if (quarter == 0 && lane == 0) {
 #pragma unroll
-        for (int h = 0; h < HG; ++h) alpha_s[h0 + h] = h0 + h < G ? alpha[h] : 0.f;
+        for (int h = 0; h < HG; ++h) alpha_s[h0 + h] = col_ok(h0 + h) ? alpha[h] : 0.f;
       }
       named_barrier_sync(1, NS);
       if (!__all_sync(0xffffffffu, wait_role(bars.cdrain, ncorr & 1, abort_flag, p.err, p.wait_limit_ns)))
@@ -779,11 +820,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (!item_valid(e)) break;
       }
       const Item it = unpack_item(e, p.part_tokens);
-      // padded heads (h >= G) get m = +inf: their scores then come out as -inf and
+      // padded heads (columns past the group) get m = +inf: their scores then come out as -inf and
       // their probabilities as 0 without a test (their l and O are never stored)
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
-        m[h] = h0 + h < G ? -INFINITY : INFINITY;
+        m[h] = col_ok(h0 + h) ? -INFINITY : INFINITY;
         lp[h] = 0.f;
       }
       for (int k = 0; k < it.nchunks; ++k, ++c) {
@@ -1002,7 +1043,7 @@ __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_co
   __shared__ int hist[kMaxChunkCounts + 1];
   __shared__ int next[kMaxChunkCounts + 1];
   const int full_chunks = p.part_tokens / kChunk;
-  const int H = p.num_kv_heads;
+  const int H = p.num_kv_heads / p.heads_per_item;  // items per (sequence, partition)
   for (int i = threadIdx.x; i <= kMaxChunkCounts; i += kListThreads) hist[i] = 0;
   __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += kListThreads) {
@@ -1070,13 +1111,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
   });
 }
 
-template <typename T, int D, int GM>
+template <typename T, int D, int GM, bool kPair = false>
 cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
-  constexpr int smem = TcLayout<D>::kSmemBytes;
+  constexpr int smem = TcLayout<kPair ? 128 : D>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // devices whose limit is raised
-  cudaError_t e = ensure_smem_limit(decode_tc_kernel<T, D, GM>, smem, configured);
+  cudaError_t e = ensure_smem_limit(decode_tc_kernel<T, D, GM, kPair>, smem, configured);
   if (e != cudaSuccess) return e;
-  return launch_dependent(decode_tc_kernel<T, D, GM>, grid, TcRoles<GM>::kThreads, smem, stream, args);
+  return launch_dependent(decode_tc_kernel<T, D, GM, kPair>, grid, TcRoles<GM>::kThreads, smem, stream, args);
 }
 
 template <typename T, int D>
@@ -1091,6 +1132,7 @@ cudaError_t launch_tc_g(const TcArgs& args, int grid, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_tc_d(const TcArgs& args, int grid, cudaStream_t stream) {
+  if (args.p.heads_per_item == 2) return launch_tc_t<T, 64, 16, true>(args, grid, stream);
   return args.p.head_dim == 64 ? launch_tc_g<T, 64>(args, grid, stream) : launch_tc_g<T, 128>(args, grid, stream);
 }
 
@@ -1115,18 +1157,27 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   }
   TcArgs args;
   args.p = p;
+  // head_dim 64: pairs of KV heads per item where the heads pair up and a pair's query
+  // heads fit the 16 columns
+  const bool pair = p.head_dim == 64 && p.num_kv_heads % 2 == 0 && p.group <= 8;
+  args.p.heads_per_item = pair ? 2 : 1;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
-  if (!make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
-      !make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, p.head_dim) ||
-      !make_map(&args.tq, p.q, static_cast<uint64_t>(p.num_seqs) * p.num_q_heads, kN, bf16, p.head_dim))
-    return cudaErrorInvalidValue;
-  const int items = p.max_parts * p.num_seqs * p.num_kv_heads;  // upper bound on the list
+  const uint64_t q_rows = static_cast<uint64_t>(p.num_seqs) * p.num_q_heads;
+  const bool maps_ok =
+      pair ? make_pair_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) &&
+                 make_pair_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) &&
+                 make_map(&args.tq, p.q, q_rows, 8, bf16, p.head_dim)
+           : make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, p.head_dim) &&
+                 make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, p.head_dim) &&
+                 make_map(&args.tq, p.q, q_rows, kN, bf16, p.head_dim);
+  if (!maps_ok) return cudaErrorInvalidValue;
+  const int items = p.max_parts * p.num_seqs * (p.num_kv_heads / args.p.heads_per_item);  // upper bound on the list
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = items < sms ? items : sms;
-  cudaError_t e = bf16 ? launch_dependent(work_list_kernel<__nv_bfloat16>, 1, kListThreads, 0, stream, p)
-                       : launch_dependent(work_list_kernel<__half>, 1, kListThreads, 0, stream, p);
+  cudaError_t e = bf16 ? launch_dependent(work_list_kernel<__nv_bfloat16>, 1, kListThreads, 0, stream, args.p)
+                       : launch_dependent(work_list_kernel<__half>, 1, kListThreads, 0, stream, args.p);
   if (e != cudaSuccess || grid == 0) return e;
   return bf16 ? launch_tc_d<__nv_bfloat16>(args, grid, stream) : launch_tc_d<__half>(args, grid, stream);
 }

@@ -30,6 +30,7 @@ struct DecodeParams {
   int32_t out_f32;   // 1: out is fp32, 0: out has the cache dtype
   float scale_log2;  // softmax scale * log2(e): scores live in the exp2 domain
   uint64_t wait_limit_ns;  // bound of every pipeline wait (kWaitLimitNs unless a test lowers it)
+  int32_t heads_per_item;  // KV heads of one tensor-core work item: 1, or 2 (head_dim 64, paired heads)
 };
 
 // Multi-token causal (prefill) attention, tensor cores; f16/bf16, head_dim 64 or 128.

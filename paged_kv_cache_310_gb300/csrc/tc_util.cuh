@@ -276,6 +276,31 @@ bool make_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t blo
   });
 }
 
+// Head_dim 64, two adjacent KV heads per box: their tiles of one block are
+// consecutive (bs rows of 128 bytes each), and the box takes row r of both as one
+// 256-byte operand row, head h's 64 columns as column block 0 and head h + 1's as
+// column block 1: dims (64 columns, 8 rows, 2 heads, 8-row groups), so one box lands
+// in shared memory exactly like a head_dim-128 tile.  The box at group w (w = the
+// first row of head h's tile / 8, h even) covers the block's bs rows of both heads.
+bool make_pair_pool_map_uncached(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows % 8 || block_size % 8) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(block_size) * 128, 1024};
+  cuuint32_t box[4] = {64, 8, 2, block_size / 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_pair_pool_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t block_size, bool bf16) {
+  return cached_map(m, MapKey{base, rows, block_size, 5, bf16 ? 2 : 1, 64}, [&](CUtensorMap* out) {
+    return make_pair_pool_map_uncached(out, base, rows, block_size, bf16);
+  });
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -306,17 +306,21 @@ def test_head_dim_64_empty_single_and_split(path):
                 assert same_bytes(got[s_, h], vc[b, h // 8, 0])
 
 
-@pytest.mark.parametrize("head_dim", [128, 64], ids=["claimed_items", "fixed_order"])
+@pytest.mark.parametrize("head_dim,num_kv_heads", [(128, 4), (64, 4), (64, 1)],
+                         ids=["claimed_items", "paired_heads", "fixed_order"])
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS.get)
-def test_all_contexts_empty(path, head_dim):
+def test_all_contexts_empty(path, head_dim, num_kv_heads):
     """No sequence has a token: the work list is empty, so every CTA of the tensor-core
-    kernel finds the end of the list at once (by claim at head_dim 128, in the fixed
-    order at 64), and every output row is zero."""
+    kernel finds the end of the list at once (by claim with head_dim-128 operands,
+    paired head_dim-64 heads included; in the fixed order at head_dim 64 with 16 query
+    heads per KV head), and every output row is zero."""
+    if not supported(path, torch.bfloat16, head_dim, 16 // num_kv_heads):
+        pytest.skip("outside this path's supported set")
     ctx = [0] * 5
     keys, owned = workloads.private_layout(ctx, 16)
     w = workloads.build_from_layout(name="all empty", seed=310_471, dtype="bf16", num_q_heads=16,
-                                    num_kv_heads=4, head_dim=head_dim, block_size=16, ctx=ctx, block_keys=keys,
-                                    owned_rows=owned, cow=[], num_blocks=3, canary=True,
+                                    num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=16, ctx=ctx,
+                                    block_keys=keys, owned_rows=owned, cow=[], num_blocks=3, canary=True,
                                     gen=torch.Generator().manual_seed(310_471))
     ref, kc, vc = oracle_step(w)
     out, g = gpu_step(w, torch.float32, path=path)
@@ -328,13 +332,41 @@ def test_all_contexts_empty(path, head_dim):
 @pytest.mark.parametrize("head_dim", [128, 64])
 def test_running_max_rising_tensor_core_shapes(head_dim, group):
     """The rescale of O in tensor memory at both head sizes and at 1, 8 and 16 query
-    heads per KV head: the head_dim-64 O buffer holds the two 64-token halves in
-    separate columns, and the columns each softmax warp rescales depend on the group."""
+    heads per KV head: at head_dim 64 with 16 the O buffer holds the two 64-token
+    halves in separate columns, with 1 and 8 an item covers two KV heads (paired heads),
+    and the columns each softmax warp rescales depend on the group."""
     w = rising_scores_workload("bf16", head_dim=head_dim, num_q_heads=2 * group, num_kv_heads=2)
     ref, kc, vc = oracle_step(w)
     out, g = gpu_step(w, torch.float32, path=pkv.PATH_TENSOR_CORE)
     check_close(out, ref, w.dtype)
     low = decode_only(w, g, w.dtype, path=pkv.PATH_TENSOR_CORE)
+    check_in_dtype(low, ref)
+    check_rounded(low, out)
+
+
+PAIRED = [
+    # dtype, bs, Hq, Hkv, max_len, part: head_dim 64 with an even number of KV heads and
+    # up to 8 query heads per KV head, where a tensor-core item covers two KV heads
+    ("bf16", 16, 4, 4, 1500, 0), ("f16", 8, 12, 6, 900, 256), ("bf16", 32, 8, 2, 2100, 128),
+    ("f16", 64, 64, 8, 1300, 0), ("bf16", 16, 6, 2, 700, 384), ("f16", 16, 40, 8, 3000, 512),
+    ("bf16", 8, 2, 2, 130, 0),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[f"{c[0]}-bs{c[1]}-{c[2]}x{c[3]}-L{c[4]}-p{c[5]}" for c in PAIRED])
+def test_paired_heads_parity(case):
+    """head_dim 64 on tensor cores with two KV heads per item: each query head's output
+    comes from its own KV head only (the query operand's off-diagonal blocks are zero,
+    the cross-term blocks of O are never read), for groups of 1 to 8 query heads
+    (including odd ones), block sizes 8 to 64, whole sequences and split partitions."""
+    dt, bs, Hq, Hkv, max_len, part = case
+    w = workloads.random_workload(310_480 + PAIRED.index(case), num_seqs=6, max_len=max_len, min_len=1,
+                                  num_q_heads=Hq, num_kv_heads=Hkv, head_dim=64, block_size=bs, dtype=dt)
+    ref, kc, vc = oracle_step(w)
+    out, g = gpu_step(w, torch.float32, path=pkv.PATH_TENSOR_CORE, part=part)
+    assert same_bytes(g.k_cache, kc) and same_bytes(g.v_cache, vc)
+    check_close(out, ref, w.dtype)
+    low = decode_only(w, g, w.dtype, path=pkv.PATH_TENSOR_CORE, part=part)
     check_in_dtype(low, ref)
     check_rounded(low, out)
 
