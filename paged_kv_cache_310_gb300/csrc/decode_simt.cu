@@ -86,6 +86,9 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   const int part = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = p.group;
+  // with partitions the next kernel is this call's merge, which waits for this grid
+  // before it reads anything: let it launch once every CTA here has started
+  if (p.max_parts > 1) grid_dependents_launch();
   const int L = p.context_lens[s];
   if (L < 0 || L > p.max_parts * p.part_tokens) {
     if (part == 0 && threadIdx.x == 0) set_error(p.err, kErrLength);
@@ -328,9 +331,12 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   }
 }
 
+// One CTA per (query head, sequence), launched as a programmatic dependent of the
+// partition kernel: it may be resident while that kernel runs and waits for it here.
 template <typename T>
 __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ DecodeParams p) {
-  const int h = blockIdx.x, s = blockIdx.y;
+  grid_dependency_wait();
+  const int h = blockIdx.x % p.num_q_heads, s = blockIdx.x / p.num_q_heads;
   const int L = p.context_lens[s];
   if (L < 0 || L > p.max_parts * p.part_tokens) return;
   const int np = (L + p.part_tokens - 1) / p.part_tokens;
@@ -388,13 +394,12 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t st
 
 cudaError_t launch_merge(const DecodeParams& p, int dtype, cudaStream_t stream) {
   if (p.max_parts <= 1) return cudaSuccess;
-  dim3 grid(p.num_q_heads, p.num_seqs);
+  const int grid = p.num_q_heads * p.num_seqs;  // (query head, sequence), head fastest
   switch (dtype) {
-    case PKV_F32: merge_kernel<float><<<grid, 128, 0, stream>>>(p); break;
-    case PKV_F16: merge_kernel<__half><<<grid, 128, 0, stream>>>(p); break;
-    default: merge_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(p); break;
+    case PKV_F32: return launch_dependent(merge_kernel<float>, grid, 128, 0, stream, p);
+    case PKV_F16: return launch_dependent(merge_kernel<__half>, grid, 128, 0, stream, p);
+    default: return launch_dependent(merge_kernel<__nv_bfloat16>, grid, 128, 0, stream, p);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

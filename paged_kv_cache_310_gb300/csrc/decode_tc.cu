@@ -341,6 +341,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   // everything above touches only this CTA; the list, the pool and q are read after
   // the preceding kernels on the stream have completed and their writes are visible.
   grid_dependency_wait();
+  // with partitions the next kernel is this call's merge, which waits for this grid
+  // before it reads anything: let it launch now, so its start overlaps this kernel
+  if (p.max_parts > 1) grid_dependents_launch();
   const int num_items = *p.work_count;
 
   if (warp == 4) {
