@@ -13,10 +13,12 @@
 // few percent of the tensor cores:
 //   S^T[128 tokens x 16] = K[128 x D dims] . Q^T[D x 16]          (QK, M=128 N=16)
 //   O^T[D dims x N]      = V^T[D dims x 128 tokens] . P^T[128 x N] (PV, M=128)
-// The query heads of a group are the N dimension of QK (padded to 16).  PV's columns
-// hold each head's probabilities twice, as a rounded part and its remainder (16
-// columns up to 8 heads, 32 up to 16).  At D = 64 one PV tile of M = 128 rows covers
-// the chunk's two 64-token halves (see PvGeom), so PV reads each V element once.
+// The query heads of a group are the N dimension of QK (padded to 16; 32 for two
+// paired heads' groups of 9 to 16).  PV's columns hold each head's probabilities twice,
+// as a rounded part and its remainder (16 columns up to 8 heads, twice the S columns
+// beyond).  At D = 64 two KV heads share an item where they pair up (see kPair);
+// otherwise one PV tile of M = 128 rows covers the chunk's two 64-token halves (see
+// PvGeom), so PV reads each V element once.
 // PV accumulates an item's chunks in tensor memory (one O buffer per item, two
 // buffers); the softmax warps read O once per item.
 //
@@ -28,14 +30,14 @@
 // order (see kClaimItems).
 // The kernel is launched as a programmatic dependent of the list kernel.  224 threads
 // (352 from 4 query heads per KV head, 608 at 16) in five roles:
-//  * warp 4, producer of Q and K (and, at D = 128, the item claims): per 128-token
-//    chunk, one lane per physical block
-//    reads the block id (before waiting for a free stage, hiding its latency) and
-//    issues one tiled TMA load of the block's K tile for this KV head (4-D box,
-//    128-byte swizzle) into a 96 KB K ring (3 stages at D = 128, 6 at D = 64); blocks
-//    past the item's end are loaded from outside the tensor, which the TMA unit fills
-//    with zeros.  It also loads the item's 16 query rows.
-//  * warp 6, producer of V: the same for V tiles into a V ring of the same size.  The
+//  * warp 4, producer of Q and K (and, with head_dim-128 operands, the item claims):
+//    per 128-token chunk, one lane per physical block reads the block id (before
+//    waiting for a free stage, hiding its latency) and issues one tiled TMA load of the
+//    block's K tile for this KV head (4-D box, 128-byte swizzle) into a K ring (3
+//    stages of 32 KB at D = 128, 6 of 16 KB at D = 64; 2 of 32 KB with 32 S columns,
+//    see TcLayout); blocks past the item's end are loaded from outside the tensor,
+//    which the TMA unit fills with zeros.  It also loads the item's query rows.
+//  * warp 6, producer of V: the same for V tiles into a 96 KB V ring.  The
 //    rings are separate so that a K stage is reused as soon as its chunk's QK
 //    completes, long before the chunk's V is done with: more of the rings stays in
 //    flight, and the kernel is bound by bytes in flight.
@@ -72,14 +74,16 @@ namespace pkv {
 namespace {
 
 constexpr int kChunk = 128;                    // tokens per MMA tile (M of QK)
-constexpr int kN = 16;                         // MMA N: query heads per group, padded
-constexpr int kQHalfBytes = kN * 128;          // 16 query rows x one 64-dimension block
+constexpr int kMaxGroup = 16;                  // query heads per KV head on this path
+// QK's N (S columns): 16, the query heads of a group padded; 32 for paired heads with
+// 16 query heads per KV head (GM = 32: the two heads' groups side by side)
+template <int GM>
+constexpr int kNCols = GM <= 16 ? 16 : 32;
 // P^T holds each probability as two rounded parts, hi = round(p) and
 // lo = round(p - hi), as separate groups of 8 columns: the PV MMA then sums
 // hi + lo in fp32, so rounding p to 16 bits costs about 2^-17 relative instead of
 // 2^-9.  Up to 8 heads: [hi 0-7][lo 0-7] (16 columns, the columns are there anyway);
 // up to 16: [hi 0-7][hi 8-15][lo 0-7][lo 8-15] (32 columns).
-constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 columns x 128 tokens
 
 // PV geometry.  At D = 128, PV is O^T[128 dims x NP] = V^T . P^T over the chunk's
 // 128 tokens (8 MMAs of K = 16) and P^T's column groups hold all 128 tokens.  At
@@ -94,14 +98,18 @@ constexpr int kPBytes = 4 * kChunk * 16;       // 8 KB: up to four groups of 8 c
 template <int D, int GM>
 struct PvGeom {
   static constexpr bool kHalves = D == 64;
-  static constexpr int kNP = GM <= 8 ? 16 : 32;          // P columns: heads' hi, then lo parts
+  static constexpr int kN = kNCols<GM>;
+  static constexpr int kNP = GM <= 8 ? 16 : 2 * kN;      // P columns: heads' hi, then lo parts
   static constexpr int kNO = kHalves ? 2 * kNP : kNP;    // N of PV: O columns per buffer
   static constexpr int kPTok = kHalves ? 64 : kChunk;    // tokens per P column group
   static constexpr int kPGroupBytes = kPTok * 16;
   static constexpr int kSteps = kPTok / 16;              // PV MMAs per chunk
-  // tensor memory: S[2] at 0/16, O[2] at 32 and 32 + kNO
-  static constexpr uint32_t kTmemCols = 32 + 2 * kNO <= 128 ? 128 : 256;
+  // one P buffer: up to 2 kN / 8 groups of 8 columns x 128 tokens (8 or 16 KB)
+  static constexpr int kPBytes = 4 * kChunk * kN;
+  // tensor memory: S[2] at 0 and kN, O[2] at 2 kN and 2 kN + kNO
+  static constexpr uint32_t kTmemCols = 2 * kN + 2 * kNO <= 128 ? 128 : 256;
   static_assert(kNP / 8 * (kHalves ? 2 : 1) * kPGroupBytes <= kPBytes, "P buffer");
+  static_assert(2 * kN + 2 * kNO <= 256, "tensor memory");
 };
 
 // Roles: warps 0-3 softmax, 4 producer of Q and K, 5 MMA, 6 producer of V, and from
@@ -112,7 +120,7 @@ struct PvGeom {
 template <int GM>
 struct TcRoles {
   // softmax warps per lane quarter (four at 16 heads: +2.5 % at head_dim 64 over two)
-  static constexpr int kSplit = GM >= 16 ? 4 : GM >= 4 ? 2 : 1;
+  static constexpr int kSplit = GM >= 16 ? 4 : GM >= 4 ? 2 : 1;  // 32 columns: 8 heads a thread
   static constexpr int kHeads = GM / kSplit;          // query heads per softmax thread
   static constexpr int kSoftmaxThreads = 128 * kSplit;
   static constexpr int kThreads = kSoftmaxThreads + 96;
@@ -133,18 +141,19 @@ constexpr int kItemRing = 8;
 template <int D>
 constexpr bool kClaimItems = D == 128;
 
-// Paired heads (head_dim 64, an even number of KV heads, up to 8 query heads per KV
-// head): a work item covers KV heads 2i and 2i + 1.  In the pool their tiles of a block
-// are adjacent, so one TMA box lands row r of both as one 256-byte operand row (head
-// 2i's 64 dimensions as column block 0, head 2i + 1's as block 1), the head_dim-128
-// shared-memory layout, and the item runs the head_dim-128 pipeline: 32 KB chunks and
-// the 16-column geometry.  QK's query operand is block diagonal: columns 0-7 hold the
-// first head's query rows in dimension block 0 (zeros in block 1), columns 8-15 the
-// second head's in block 1, so each S column sees its own head's K only.  PV computes
-// O^T = V^T . P^T over all 128 rows; rows 0-63 (the first head's dimensions) are read
-// in columns 0-7 and rows 64-127 in columns 8-15, the other two blocks are cross terms
-// nobody reads.  With 16 KB chunks of one head the per-chunk costs (barrier round
-// trips, the softmax pass, item changes) weigh twice as much per byte.
+// Paired heads (head_dim 64, an even number of KV heads): a work item covers KV heads
+// 2i and 2i + 1.  In the pool their tiles of a block are adjacent, so one TMA box lands
+// row r of both as one 256-byte operand row (head 2i's 64 dimensions as column block 0,
+// head 2i + 1's as block 1), the head_dim-128 shared-memory layout, and the item runs
+// the head_dim-128 pipeline with 32 KB chunks.  QK's query operand is block diagonal:
+// the first half of the S columns (8 up to 8 query heads per KV head, else 16: GM = 16
+// or 32) holds the first head's query rows in dimension block 0 (zeros in block 1), the
+// second half the second head's in block 1, so each S column sees its own head's K
+// only.  PV computes O^T = V^T . P^T over all 128 rows; rows 0-63 (the first head's
+// dimensions) are read in the first half of the columns and rows 64-127 in the second,
+// the other two blocks are cross terms nobody reads.  With 16 KB chunks of one head the
+// per-chunk costs (barrier round trips, the softmax pass, item changes) weigh twice as
+// much per byte.
 
 __device__ __forceinline__ bool item_valid(int4 e) { return (e.w & 0xffff) != 0; }  // ntok 0 = end
 
@@ -155,20 +164,27 @@ __device__ __forceinline__ bool item_valid(int4 e) { return (e.w & 0xffff) != 0;
 // groups kGroupBytes apart, 64-dimension blocks 1 KB apart), and one 4-D TMA box fills
 // a whole block.  K and V have separate rings: a K stage is free once the chunk's QK
 // completed, long before its V (needed until PV completes), so more of the rings stays
-// in flight; each ring holds 96 KB whatever D is.
-template <int D>
+// in flight; each ring holds 96 KB whatever D is, except that with 32 S columns the
+// doubled query and probability buffers take one K stage's room (64 KB of K: a K stage
+// is held only until its QK completes, a V stage until PV; two V stages measured 1-3 %
+// slower at 16 query heads per KV head).
+template <int D, int GM>
 struct TcLayout {
+  static constexpr int kN = kNCols<GM>;
+  static constexpr int kQHalfBytes = kN * 128;           // the query rows x one 64-dimension block
   static constexpr int kBlocks = D / 64;                 // 64-column blocks of a row
   static constexpr int kGroupBytes = 8 * D * 2;          // one 8-row group: all its blocks
   static constexpr int kTileBytes = kChunk * D * 2;      // K or V of one chunk: 16 or 32 KB
-  static constexpr int kStages = 3 * 128 / D;            // per ring
+  static constexpr int kKStages = (kN == 32 ? 2 : 3) * 128 / D;  // K ring
+  static constexpr int kVStages = 3 * 128 / D;                   // V ring
   static constexpr int kQBytes = kBlocks * kQHalfBytes;  // the item's query rows
-  static constexpr int kOffV = kStages * kTileBytes;
-  static constexpr int kOffQ = 2 * kStages * kTileBytes;
+  static constexpr int kPBytes = PvGeom<D, GM>::kPBytes;
+  static constexpr int kOffV = kKStages * kTileBytes;
+  static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
   static constexpr int kOffP = kOffQ + 2 * kQBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
   // rings (K, V: full, empty), 8 pairs, rescale handshake (2), drain, item ring
-  static constexpr int kNumBars = 4 * kStages + 8 * 2 + 3 + 2 * kItemRing;
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 8 * 2 + 3 + 2 * kItemRing;
   static constexpr int kOffRedMax = kOffBar + kNumBars * 8;
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * kN * 4;  // [2 item slots][4 warps][kN]
   static constexpr int kOffMTot = kOffRedL + 2 * 4 * kN * 4;    // [2 item slots][kN]
@@ -202,16 +218,16 @@ struct Bars {
   uint64_t* iempty; // [kItemRing] slot read by every other role
 };
 
-template <int D>
+template <int D, int GM>
 __device__ __forceinline__ Bars carve_bars(unsigned char* smem) {
-  constexpr int S = TcLayout<D>::kStages;
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem + TcLayout<D>::kOffBar);
+  using L = TcLayout<D, GM>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   Bars r;
   r.kfull = b;
-  r.kempty = b + S;
-  r.vfull = b + 2 * S;
-  r.vempty = b + 3 * S;
-  r.qfull = b + 4 * S;
+  r.kempty = b + L::kKStages;
+  r.vfull = b + 2 * L::kKStages;
+  r.vempty = r.vfull + L::kVStages;
+  r.qfull = r.vempty + L::kVStages;
   r.qempty = r.qfull + 2;
   r.sfull = r.qempty + 2;
   r.sfree = r.sfull + 2;
@@ -252,15 +268,17 @@ __device__ __forceinline__ Item unpack_item(int4 e, int part_tokens) {
   return it;
 }
 
-// kPair (head_dim D = 64, up to 8 query heads per KV head): an item covers two
-// adjacent KV heads and runs with head_dim-128 operands (see the paired-heads note above).
+// kPair (head_dim D = 64, an even number of KV heads): an item covers two adjacent KV
+// heads and runs with head_dim-128 operands (see the paired-heads note above).
 template <typename T, int D, int GM, bool kPair>
 __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(const __grid_constant__ TcArgs a) {
-  static_assert(!kPair || (D == 64 && GM == 16), "paired heads: head_dim 64, the 16-column geometry");
+  static_assert(kPair ? D == 64 && (GM == 16 || GM == 32) : GM <= 16, "paired heads: head_dim 64");
   constexpr int DL = kPair ? 128 : D;  // operand width: dimensions of a K/V row in shared memory
-  using L = TcLayout<DL>;
+  using L = TcLayout<DL, GM>;
   using R = TcRoles<GM>;
-  constexpr int kKStages = L::kStages, kVStages = L::kStages;
+  constexpr int kKStages = L::kKStages, kVStages = L::kVStages;
+  constexpr int kN = L::kN, kQHalfBytes = L::kQHalfBytes, kPBytes = L::kPBytes;
+  constexpr int kHalfCols = kN / 2;  // paired: the columns of each head's group
   constexpr int kGroupBytes = L::kGroupBytes, kTileBytes = L::kTileBytes, kQBytes = L::kQBytes;
   constexpr int kOffV = L::kOffV, kOffQ = L::kOffQ, kOffP = L::kOffP;
   using PG = PvGeom<DL, GM>;
@@ -270,7 +288,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   extern __shared__ __align__(1024) unsigned char smem[];
   const DecodeParams& p = a.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const Bars bars = carve_bars<DL>(smem);
+  const Bars bars = carve_bars<DL, GM>(smem);
   float* red_max = reinterpret_cast<float*>(smem + L::kOffRedMax);  // [2][4 warps][kN]
   float* red_l = reinterpret_cast<float*>(smem + L::kOffRedL);      // [2 item slots][4 warps][kN]
   float* red_mtot = reinterpret_cast<float*>(smem + L::kOffMTot);   // [2 item slots][kN]
@@ -284,9 +302,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
   volatile int* cflag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 20);  // [2] rescale before PV
   int4* ring = reinterpret_cast<int4*>(smem + L::kOffRing);
   const int G = p.group;
-  // S/O column n holds a query head of the item: n < G; paired, n % 8 < G (the first
-  // head's group in columns 0-7, the second's in 8-15)
-  auto col_ok = [G](int n) { return kPair ? (n & 7) < G : n < G; };
+  // S/O column n holds a query head of the item: n < G; paired, n % (kN / 2) < G (the
+  // first head's group in the first half of the columns, the second's in the second)
+  auto col_ok = [G](int n) { return kPair ? n % kHalfCols < G : n < G; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -406,12 +424,13 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (ok) {
           unsigned char* qdst = smem + kOffQ + qb * kQBytes;
           if constexpr (kPair) {
-            // 8 query rows from the first head's group into rows 0-7 of dimension block
-            // 0, 8 from the second's into rows 8-15 of block 1 (box 64 x 8)
+            // kN / 2 query rows from the first head's group into the first rows of
+            // dimension block 0, kN / 2 from the second's into the rows after them in
+            // block 1 (box 64 x kN / 2; rows past a group belong to no column that is read)
             const int qrow = it.s * p.num_q_heads + it.g * 2 * G;
-            mbar_arrive_expect_tx(&bars.qfull[qb], 2 * 8 * 128);
+            mbar_arrive_expect_tx(&bars.qfull[qb], 2 * kHalfCols * 128);
             tma_load_2d(qdst, &a.tq, 0, qrow, &bars.qfull[qb], pol_keep);
-            tma_load_2d(qdst + kQHalfBytes + 8 * 128, &a.tq, 0, qrow + G, &bars.qfull[qb], pol_keep);
+            tma_load_2d(qdst + kQHalfBytes + kHalfCols * 128, &a.tq, 0, qrow + G, &bars.qfull[qb], pol_keep);
           } else {
             const int qrow = it.s * p.num_q_heads + it.g * G;
             mbar_arrive_expect_tx(&bars.qfull[qb], kQBytes);
@@ -594,7 +613,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < PG::kSteps; ++kk)
-            mma_f16(tmem + 32 + ob * kNO, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
+            mma_f16(tmem + 2 * kN + ob * kNO, dv + ((kk * 2 * kGroupBytes) >> 4), dp + ((kk * 256) >> 4), idesc_pv,
                     kk > 0 || pk > 0);
           mma_commit(&bars.pfree[pb]);
           mma_commit(&bars.vempty[pst]);
@@ -627,7 +646,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           for (int kk = 0; kk < DL / 16; ++kk) {
             const uint32_t ko = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
             const uint32_t qo = ((kk >> 2) * kQHalfBytes + (kk & 3) * 32) >> 4;
-            mma_f16(tmem + sb * 16, dk + ko, dq + qo, idesc_qk, kk > 0);
+            mma_f16(tmem + sb * kN, dk + ko, dq + qo, idesc_qk, kk > 0);
           }
           mma_commit(&bars.sfull[sb]);
           mma_commit(&bars.kempty[qst]);           // the K stage is free once this QK completed
@@ -699,7 +718,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         tc_fence_after();
         // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16; at D = 64
         // rows 64-127 hold the chunks' second halves in the next NP columns
-        const uint32_t oaddr = lane_base + 32 + ob * kNO + (PG::kHalves && quarter >= 2 ? PG::kNP : 0) + h0;
+        const uint32_t oaddr = lane_base + 2 * kN + ob * kNO + (PG::kHalves && quarter >= 2 ? PG::kNP : 0) + h0;
         float olo[HG];
         if (GM <= 8) {  // 4-column aligned loads; a pair at column 2 is picked from them
           float a4[4], b4[4];
@@ -710,9 +729,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
             olo[h] = (h0 & 2) ? b4[(2 + h) & 3] : b4[h];
           }
         } else if (HG == 4) {
-          tmem_load4x2(oaddr, oaddr + 16, o, olo);
+          tmem_load4x2(oaddr, oaddr + PG::kNP / 2, o, olo);
         } else {
-          tmem_load8x2(oaddr, oaddr + 16, o, olo);
+          tmem_load8x2(oaddr, oaddr + PG::kNP / 2, o, olo);
         }
         tc_fence_before();
         __syncwarp();
@@ -744,11 +763,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           const int n = h0 + h;
-          if (col_ok(n) && (!kPair || (n >> 3) == (t >> 6))) {
+          if (col_ok(n) && (!kPair || n / kHalfCols == (t >> 6))) {
             const float acc = o[h];
             const float l = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
             const size_t row = static_cast<size_t>(pend_s) * p.num_q_heads +
-                               (kPair ? pend_g * 2 * G + (n >> 3) * G + (n & 7) : pend_g * G + n);
+                               (kPair ? pend_g * 2 * G + (n / kHalfCols) * G + n % kHalfCols : pend_g * G + n);
             if (pend_nparts == 1) {
               store_out<T>(p.out, row * D + dim, acc / l, p.out_f32);
             } else {
@@ -782,7 +801,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       // O columns: per half, the heads' hi parts then their lo parts
       constexpr int kCols = kNO / R::kSplit;   // this warp's share of its lane quarter: 8 to 32
       const int c0 = (h0 / HG) * kCols;
-      const uint32_t oaddr = lane_base + 32 + ob * kNO + c0;
+      const uint32_t oaddr = lane_base + 2 * kN + ob * kNO + c0;
 #pragma unroll
       for (int q = 0; q < kCols / 8; ++q) {
         float v[8];
@@ -841,11 +860,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           tc_fence_after();
           if (HG <= 4) {  // 4-column aligned load; a pair at column 2 is picked from it
             float s4[4];
-            tmem_load4(lane_base + sb * 16 + (h0 & ~3), s4);
+            tmem_load4(lane_base + sb * kN + (h0 & ~3), s4);
 #pragma unroll
             for (int h = 0; h < HG; ++h) sv[h] = (h0 & 2) ? s4[(2 + h) & 3] : s4[h];
           } else {
-            tmem_load8(lane_base + sb * 16 + h0, sv);
+            tmem_load8(lane_base + sb * kN + h0, sv);
           }
           tc_fence_before();
           __syncwarp();
@@ -935,11 +954,11 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         } else if (HG == 4) {  // 16 heads over four warps: each writes half of a column group
           const int gh = h0 / 8, off = (h0 & 7) * 2;
           *reinterpret_cast<uint2*>(pdst + gh * kGB + off) = make_uint2(hw[0], hw[1]);
-          *reinterpret_cast<uint2*>(pdst + (2 + gh) * kGB + off) = make_uint2(lw[0], lw[1]);
+          *reinterpret_cast<uint2*>(pdst + (PG::kNP / 16 + gh) * kGB + off) = make_uint2(lw[0], lw[1]);
         } else {
           const int gh = h0 / 8;  // this warp's column group of hi parts
           *reinterpret_cast<uint4*>(pdst + gh * kGB) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(pdst + (2 + gh) * kGB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(pdst + (PG::kNP / 16 + gh) * kGB) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         // rows of the last loaded block past the context end: zero their V rows (only an
         // item's last chunk can have them; the first warp of each quarter does it)
@@ -1116,7 +1135,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 
 template <typename T, int D, int GM, bool kPair = false>
 cudaError_t launch_tc_t(const TcArgs& args, int grid, cudaStream_t stream) {
-  constexpr int smem = TcLayout<kPair ? 128 : D>::kSmemBytes;
+  constexpr int smem = TcLayout<kPair ? 128 : D, GM>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};  // devices whose limit is raised
   cudaError_t e = ensure_smem_limit(decode_tc_kernel<T, D, GM, kPair>, smem, configured);
   if (e != cudaSuccess) return e;
@@ -1135,14 +1154,16 @@ cudaError_t launch_tc_g(const TcArgs& args, int grid, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_tc_d(const TcArgs& args, int grid, cudaStream_t stream) {
-  if (args.p.heads_per_item == 2) return launch_tc_t<T, 64, 16, true>(args, grid, stream);
+  if (args.p.heads_per_item == 2)
+    return args.p.group <= 8 ? launch_tc_t<T, 64, 16, true>(args, grid, stream)
+                             : launch_tc_t<T, 64, 32, true>(args, grid, stream);
   return args.p.head_dim == 64 ? launch_tc_g<T, 64>(args, grid, stream) : launch_tc_g<T, 128>(args, grid, stream);
 }
 
 }  // namespace
 
 bool tc_supported(int dtype, int head_dim, int group, int block_size) {
-  const int max_group = dtype == PKV_F32 ? 8 : kN;  // f32: the tf32 kernel's N holds 8 heads twice
+  const int max_group = dtype == PKV_F32 ? 8 : kMaxGroup;  // f32: the tf32 kernel's N holds 8 heads twice
   return (dtype == PKV_F16 || dtype == PKV_BF16 || dtype == PKV_F32) && (head_dim == 64 || head_dim == 128) &&
          group >= 1 && group <= max_group &&
          (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64);
@@ -1160,9 +1181,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   }
   TcArgs args;
   args.p = p;
-  // head_dim 64: pairs of KV heads per item where the heads pair up and a pair's query
-  // heads fit the 16 columns
-  const bool pair = p.head_dim == 64 && p.num_kv_heads % 2 == 0 && p.group <= 8;
+  // head_dim 64: pairs of KV heads per item wherever the KV heads pair up (16 S columns
+  // up to 8 query heads per KV head, 32 beyond)
+  const bool pair = p.head_dim == 64 && p.num_kv_heads % 2 == 0;
   args.p.heads_per_item = pair ? 2 : 1;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;
@@ -1170,10 +1191,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   const bool maps_ok =
       pair ? make_pair_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16) &&
                  make_pair_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16) &&
-                 make_map(&args.tq, p.q, q_rows, 8, bf16, p.head_dim)
+                 make_map(&args.tq, p.q, q_rows, p.group <= 8 ? 8 : 16, bf16, p.head_dim)
            : make_pool_map(&args.tk, p.k_cache, pool_rows, p.block_size, bf16, p.head_dim) &&
                  make_pool_map(&args.tv, p.v_cache, pool_rows, p.block_size, bf16, p.head_dim) &&
-                 make_map(&args.tq, p.q, q_rows, kN, bf16, p.head_dim);
+                 make_map(&args.tq, p.q, q_rows, kNCols<16>, bf16, p.head_dim);
   if (!maps_ok) return cudaErrorInvalidValue;
   const int items = p.max_parts * p.num_seqs * (p.num_kv_heads / args.p.heads_per_item);  // upper bound on the list
   const int sms = sm_count();

@@ -328,14 +328,16 @@ def test_all_contexts_empty(path, head_dim, num_kv_heads):
     check_close(out, ref, w.dtype)
 
 
-@pytest.mark.parametrize("group", [1, 8, 16])
+@pytest.mark.parametrize("group,num_kv_heads", [(1, 2), (8, 2), (16, 2), (16, 1)])
 @pytest.mark.parametrize("head_dim", [128, 64])
-def test_running_max_rising_tensor_core_shapes(head_dim, group):
+def test_running_max_rising_tensor_core_shapes(head_dim, group, num_kv_heads):
     """The rescale of O in tensor memory at both head sizes and at 1, 8 and 16 query
-    heads per KV head: at head_dim 64 with 16 the O buffer holds the two 64-token
-    halves in separate columns, with 1 and 8 an item covers two KV heads (paired heads),
-    and the columns each softmax warp rescales depend on the group."""
-    w = rising_scores_workload("bf16", head_dim=head_dim, num_q_heads=2 * group, num_kv_heads=2)
+    heads per KV head: at head_dim 64 an item covers two KV heads (16 S columns up to 8
+    query heads per KV head, 32 at 16), and with one KV head the O buffer holds the two
+    64-token halves in separate columns; the columns each softmax warp rescales depend
+    on the group."""
+    w = rising_scores_workload("bf16", head_dim=head_dim, num_q_heads=num_kv_heads * group,
+                               num_kv_heads=num_kv_heads)
     ref, kc, vc = oracle_step(w)
     out, g = gpu_step(w, torch.float32, path=pkv.PATH_TENSOR_CORE)
     check_close(out, ref, w.dtype)
@@ -350,6 +352,11 @@ PAIRED = [
     ("bf16", 16, 4, 4, 1500, 0), ("f16", 8, 12, 6, 900, 256), ("bf16", 32, 8, 2, 2100, 128),
     ("f16", 64, 64, 8, 1300, 0), ("bf16", 16, 6, 2, 700, 384), ("f16", 16, 40, 8, 3000, 512),
     ("bf16", 8, 2, 2, 130, 0),
+    # 9 to 16 query heads per KV head: 32 S columns, two K stages
+    ("bf16", 16, 32, 2, 1200, 0), ("f16", 32, 128, 8, 2000, 256), ("bf16", 8, 24, 2, 600, 128),
+    ("f16", 64, 64, 4, 900, 0),
+    # odd numbers of KV heads: one head per item (the 64-token halves of a chunk share a tile)
+    ("bf16", 16, 48, 3, 1500, 0), ("f16", 16, 16, 1, 900, 256), ("bf16", 32, 5, 5, 700, 0),
 ]
 
 
@@ -357,8 +364,9 @@ PAIRED = [
 def test_paired_heads_parity(case):
     """head_dim 64 on tensor cores with two KV heads per item: each query head's output
     comes from its own KV head only (the query operand's off-diagonal blocks are zero,
-    the cross-term blocks of O are never read), for groups of 1 to 8 query heads
-    (including odd ones), block sizes 8 to 64, whole sequences and split partitions."""
+    the cross-term blocks of O are never read), for groups of 1 to 16 query heads
+    (including odd ones; 16 or 32 S columns), block sizes 8 to 64, whole sequences and
+    split partitions; and, with an odd number of KV heads, one head per item."""
     dt, bs, Hq, Hkv, max_len, part = case
     w = workloads.random_workload(310_480 + PAIRED.index(case), num_seqs=6, max_len=max_len, min_len=1,
                                   num_q_heads=Hq, num_kv_heads=Hkv, head_dim=64, block_size=bs, dtype=dt)
