@@ -30,12 +30,20 @@ def _decode(w, g, path, part):
     return out
 
 
-@pytest.mark.parametrize("path,dtype", [(pkv.PATH_CUDA_CORE, "bf16"), (pkv.PATH_TENSOR_CORE, "bf16"),
-                                        (pkv.PATH_TENSOR_CORE, "f32")],
-                         ids=["cuda_core", "tensor_core", "tensor_core_f32"])
-def test_decode_gives_up_and_the_context_survives(path, dtype):
-    w = workloads.random_workload(310_480, num_seqs=8, max_len=2500, min_len=300, num_q_heads=16, num_kv_heads=4,
-                                  head_dim=128, block_size=16, dtype=dtype, canary=False)
+# (path, dtype, head_dim, query heads, KV heads): at head_dim 64 two KV heads share an item
+# (16 S columns at 4 query heads per KV head, 32 columns and two K stages at 16), and an
+# odd number of KV heads keeps one head per item in the fixed order
+CASES = [(pkv.PATH_CUDA_CORE, "bf16", 128, 16, 4), (pkv.PATH_TENSOR_CORE, "bf16", 128, 16, 4),
+         (pkv.PATH_TENSOR_CORE, "f32", 128, 16, 4), (pkv.PATH_TENSOR_CORE, "bf16", 64, 16, 4),
+         (pkv.PATH_TENSOR_CORE, "bf16", 64, 64, 4), (pkv.PATH_TENSOR_CORE, "bf16", 64, 48, 3)]
+
+
+@pytest.mark.parametrize("path,dtype,head_dim,hq,hkv", CASES,
+                         ids=["cuda_core", "tensor_core", "tensor_core_f32", "tensor_core_d64_paired",
+                              "tensor_core_d64_paired_32cols", "tensor_core_d64_one_head"])
+def test_decode_gives_up_and_the_context_survives(path, dtype, head_dim, hq, hkv):
+    w = workloads.random_workload(310_480, num_seqs=8, max_len=2500, min_len=300, num_q_heads=hq, num_kv_heads=hkv,
+                                  head_dim=head_dim, block_size=16, dtype=dtype, canary=False)
     g = w.to("cuda")
     assert pkv.device_error() == 0
     pkv.set_wait_limit(FORCED_LIMIT_NS)
