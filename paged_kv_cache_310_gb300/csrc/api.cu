@@ -104,7 +104,8 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   const bool tc_ok = tc_supported(c->dtype, c->head_dim, group, c->block_size);
   // Tensor cores wherever they apply to 16-bit caches: at G >= 2 QK and PV are real
   // contractions, and at G = 1 the persistent TMA/tcgen05 kernel still streams K/V
-  // slightly faster (0.977 vs 0.922 of copy bandwidth on a 64 x 32-head bf16 batch).
+  // faster (1.00-1.02 against 0.92 of copy bandwidth on a 64 x 32-head bf16 batch; at
+  // head_dim 64 0.91 with paired KV heads against 0.86).
   // f32 caches take the tf32 kernel from 5 query heads per KV head (at 8: 0.82 of copy
   // bandwidth against 0.36 on CUDA cores, head_dim 128); up to 4 the CUDA-core kernel
   // streams faster (0.92 against 0.84 at 4) with no conversion work.

@@ -126,18 +126,20 @@ struct TcRoles {
   static constexpr int kThreads = kSoftmaxThreads + 96;
 };
 
-// Claimed items (head_dim 128): the Q/K producer of a CTA takes the next entry of the
-// sorted list with a global atomic as it runs out of its current item, so the longest
-// items go first and whichever CTA gets free takes the next (measured with a fixed
-// snake order: per-CTA chunk counts 113-124 and per-SM speeds within about 5 % left
-// the last CTA 15-22 us behind the first).  The claimed entries reach the other
-// roles through a ring of kItemRing slots in shared memory.
+// Claimed items (head_dim-128 operands: head_dim 128, and paired heads at 64): the Q/K
+// producer of a CTA takes the next entry of the sorted list with a global atomic as it
+// runs out of its current item, so the longest items go first and whichever CTA gets
+// free takes the next (measured with a fixed snake order: per-CTA chunk counts 113-124
+// and per-SM speeds within about 5 % left the last CTA 15-22 us behind the first).  The
+// claimed entries reach the other roles through a ring of kItemRing slots in shared
+// memory.
 constexpr int kItemRing = 8;
 // At head_dim 128 claiming measured 3-4 % faster than the fixed snake order on the
 // 7B-like, GQA-70B-like and long-context workloads and 1-2 % on the shared-prefix one.
-// At head_dim 64 it measured slower in every form tried (claims early or late, items
-// read ahead, block ids read ahead, head-major list order: 0.73-0.80 against 0.76-0.83
-// of the copy bandwidth), so the fixed order stays there.
+// At head_dim 64 with one head per item it measured slower in every form tried (claims
+// early or late, items read ahead, block ids read ahead, head-major list order:
+// 0.73-0.80 against 0.76-0.83 of the copy bandwidth), so the fixed order stays there.
+// The template argument is the operand width (128 for paired heads).
 template <int D>
 constexpr bool kClaimItems = D == 128;
 
@@ -716,8 +718,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
       float o[HG];
       if (w) {
         tc_fence_after();
-        // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-15][lo 0-15] for 16; at D = 64
-        // rows 64-127 hold the chunks' second halves in the next NP columns
+        // O columns: [hi 0-7][lo 0-7] up to 8 heads, [hi][lo] of kN columns each beyond;
+        // with the 64-token halves (head_dim 64, one head per item) rows 64-127 hold the
+        // chunks' second halves in the next NP columns
         const uint32_t oaddr = lane_base + 2 * kN + ob * kNO + (PG::kHalves && quarter >= 2 ? PG::kNP : 0) + h0;
         float olo[HG];
         if (GM <= 8) {  // 4-column aligned loads; a pair at column 2 is picked from them
@@ -936,8 +939,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
           }
         }
         // P^T for PV: token t's head weights, MN-major without swizzle, 8 columns (16
-        // bytes) a group: [hi 0-7][lo 0-7] up to 8 heads, [hi 0-7][hi 8-15][lo 0-7][lo
-        // 8-15] for 16; at D = 64 those groups once per 64-token half
+        // bytes) a group: [hi 0-7][lo 0-7] up to 8 heads, then the hi groups of all kN
+        // columns followed by their lo groups; with the 64-token halves (head_dim 64, one
+        // head per item) those groups once per half
         const int tt = PG::kHalves ? (t & 63) : t;  // token within its column group
         unsigned char* pdst = smem + kOffP + sb * kPBytes + (tt >> 3) * 128 + (tt & 7) * 16 +
                               (PG::kHalves ? (t >> 6) * (PG::kNP / 8) * PG::kPGroupBytes : 0);
