@@ -402,7 +402,9 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
     if constexpr (!kDyn) {
       sc.init(p.work_list, num_items);
     } else if (lane == 0) {
-      idx = atomicAdd(p.work_next, 1);
+      // the first item is list entry blockIdx.x (the grid takes the longest ones at once,
+      // without waiting for an atomic's round trip); later claims start past the grid
+      idx = blockIdx.x;
       if (idx < num_items) e = p.work_list[idx];
       ok = publish(0, e);
     }
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(TcRoles<GM>::kThreads, 1) decode_tc_kernel(con
         if (lane == 0) {
           *kissued_slot = c + 1;
           if constexpr (kDyn) {
-            if (k == max(0, it.nchunks - 4)) idx = atomicAdd(p.work_next, 1);
+            if (k == max(0, it.nchunks - 4)) idx = static_cast<int>(gridDim.x) + atomicAdd(p.work_next, 1);
             if (k == max(0, it.nchunks - 2)) nxt = idx < num_items ? p.work_list[idx] : make_int4(0, 0, 0, 0);
             if (k == it.nchunks - 1) ok = publish(j + 1, nxt);
           }
@@ -1065,7 +1067,7 @@ constexpr int kMaxChunkCounts = kTcMaxPartition / kChunk;
 template <typename T>
 __global__ void __launch_bounds__(kListThreads) work_list_kernel(const __grid_constant__ DecodeParams p) {
   grid_dependents_launch();  // the decode kernel may start its prologue now
-  if (threadIdx.x == 0) *p.work_next = 0;  // the decode CTAs claim items from 0 on
+  if (threadIdx.x == 0) *p.work_next = 0;  // claims past the decode grid's first items
   __shared__ int hist[kMaxChunkCounts + 1];
   __shared__ int next[kMaxChunkCounts + 1];
   const int full_chunks = p.part_tokens / kChunk;

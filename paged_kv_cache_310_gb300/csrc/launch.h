@@ -23,7 +23,7 @@ struct DecodeParams {
   int* err;      // device error flag
   int4* work_list;  // tensor-core path: items sorted longest first (work-list kernel)
   int* work_count;  // number of entries in work_list
-  int* work_next;   // next entry of work_list to claim (reset by the work-list kernel)
+  int* work_next;   // claims so far past the grid's first entries (reset by the work-list kernel)
   int32_t num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq;
   int32_t block_size, num_blocks, head_dim;
   int32_t part_tokens, max_parts;
