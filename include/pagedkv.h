@@ -145,6 +145,9 @@ typedef struct {
   int32_t max_partitions;    /* partitions of the longest sequence (1 = no merge) */
   int32_t kernel_launches;   /* kernels one call enqueues */
   size_t workspace_bytes;    /* as paged_attention_workspace_bytes */
+  int32_t kv_heads_per_item; /* tensor-core path: KV heads one work item covers; 2 for f16/bf16
+                                at head_dim 64 with an even number of KV heads (their tiles of a
+                                block are adjacent and load as one head_dim-128 tile), else 1 */
 } pkv_decode_plan;
 
 /*

@@ -61,7 +61,7 @@ class DecodeConfig(ctypes.Structure):
 class DecodePlan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("partition_tokens", ctypes.c_int32),
                 ("max_partitions", ctypes.c_int32), ("kernel_launches", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("kv_heads_per_item", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

@@ -285,6 +285,8 @@ pkv_status paged_attention_plan(int32_t num_seqs, int32_t num_q_heads, int32_t m
   out->kernel_launches = num_seqs == 0 ? 0
                          : 1 + (plan.path == PKV_PATH_TENSOR_CORE ? 1 : 0) + (plan.max_parts > 1 ? 1 : 0);
   out->workspace_bytes = plan.workspace;
+  out->kv_heads_per_item =
+      plan.path == PKV_PATH_TENSOR_CORE ? tc_heads_per_item(cache->dtype, cache->head_dim, cache->num_kv_heads) : 1;
   return PKV_OK;
 }
 

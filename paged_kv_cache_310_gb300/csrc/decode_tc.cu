@@ -1175,6 +1175,12 @@ bool tc_supported(int dtype, int head_dim, int group, int block_size) {
          (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64);
 }
 
+// head_dim 64 on the 16-bit kernel: pairs of KV heads per item wherever the KV heads pair
+// up (16 S columns up to 8 query heads per KV head, 32 beyond)
+int tc_heads_per_item(int dtype, int head_dim, int num_kv_heads) {
+  return dtype != PKV_F32 && head_dim == 64 && num_kv_heads % 2 == 0 ? 2 : 1;
+}
+
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream) {
   if (dtype == PKV_F32) {  // the tf32 kernel (decode_tc32.cu) over the same work list
     const int items = p.max_parts * p.num_seqs * p.num_kv_heads;
@@ -1187,9 +1193,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stre
   }
   TcArgs args;
   args.p = p;
-  // head_dim 64: pairs of KV heads per item wherever the KV heads pair up (16 S columns
-  // up to 8 query heads per KV head, 32 beyond)
-  const bool pair = p.head_dim == 64 && p.num_kv_heads % 2 == 0;
+  const bool pair = tc_heads_per_item(dtype, p.head_dim, p.num_kv_heads) == 2;
   args.p.heads_per_item = pair ? 2 : 1;
   const bool bf16 = dtype == PKV_BF16;
   const uint64_t pool_rows = static_cast<uint64_t>(p.num_blocks) * p.num_kv_heads * p.block_size;

@@ -62,6 +62,8 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t st
 // fed by a work list that a one-CTA kernel builds first.  Partitions <= 4096 tokens.
 constexpr int kTcMaxPartition = 4096;
 bool tc_supported(int dtype, int head_dim, int group, int block_size);
+// KV heads one work item of the 16-bit tensor-core decode covers (2: paired heads).
+int tc_heads_per_item(int dtype, int head_dim, int num_kv_heads);
 cudaError_t launch_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream);
 // The f32 (tf32, split-operand) decode kernel over a work list already launched on the
 // stream; head_dim 64/128, group <= 8.

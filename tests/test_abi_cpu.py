@@ -143,6 +143,15 @@ def test_plan_reports_path_partitions_and_launches(lib):
     torch = __import__("torch")
     k16d64 = torch.empty((1, 8, 16, 64), dtype=torch.float16)
     assert pkv.paged_attention_plan(64, 8, 2048, k16d64)["path"] == pkv.PATH_TENSOR_CORE  # f16, D64
+    # head_dim 64 on the 16-bit tensor-core kernel: an even number of KV heads pairs up,
+    # two KV heads per work item (any group size); otherwise one
+    assert pkv.paged_attention_plan(64, 8, 2048, k16d64)["kv_heads_per_item"] == 2       # 8 KV heads, G = 1
+    assert pkv.paged_attention_plan(64, 128, 2048, k16d64)["kv_heads_per_item"] == 2     # G = 16
+    k16d64odd = torch.empty((1, 3, 16, 64), dtype=torch.bfloat16)
+    assert pkv.paged_attention_plan(64, 48, 2048, k16d64odd)["kv_heads_per_item"] == 1   # 3 KV heads
+    assert pkv.paged_attention_plan(64, 8, 2048, k16)["kv_heads_per_item"] == 1          # head_dim 128
+    assert pkv.paged_attention_plan(64, 64, 2048, k32)["kv_heads_per_item"] == 1          # f32, tf32 kernel
+    assert pkv.paged_attention_plan(64, 8, 2048, k16d64, path=pkv.PATH_CUDA_CORE)["kv_heads_per_item"] == 1
     k16b64 = torch.empty((1, 8, 64, 128), dtype=torch.bfloat16)
     assert pkv.paged_attention_plan(128, 8, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # 64-token blocks
     k32b64 = torch.empty((1, 8, 64, 128), dtype=torch.float32)
