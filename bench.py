@@ -661,6 +661,7 @@ def main():
                    "head_dim": D, "block_size": w.block_size, "sum_context_tokens": tokens,
                    "kv_bytes_per_step": kv_bytes, "path": {1: "cuda_core", 2: "tensor_core"}[plan["path"]],
                    "partition_tokens": plan["partition_tokens"], "partitions": plan["max_partitions"],
+                   "kv_heads_per_item": plan["kv_heads_per_item"],
                    "l2": f"inputs larger than L2 (KV {kv_bytes / 1e9:.2f} GB > 129 MB): no flush",
                    "parallelism": f"replicas x{world}", "block_tables": "identity" if args.identity_tables
                    else "shuffled"},
