@@ -97,8 +97,8 @@ typedef struct {
 } pkv_cache_desc;
 
 /* Decode path selection and split-K partition size (NULL config = automatic: tensor
- * cores for f16/bf16 with groups <= 16 and for f32 with groups 5 to 8, CUDA cores
- * otherwise). */
+ * cores for f16/bf16 with groups <= 16 and for f32 at head_dim 128 with groups 5 to 8,
+ * CUDA cores otherwise). */
 typedef enum { PKV_PATH_AUTO = 0, PKV_PATH_CUDA_CORE = 1, PKV_PATH_TENSOR_CORE = 2 } pkv_path;
 
 typedef struct {

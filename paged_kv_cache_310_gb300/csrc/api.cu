@@ -106,11 +106,13 @@ pkv_status plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t max_len,
   // contractions, and at G = 1 the persistent TMA/tcgen05 kernel still streams K/V
   // faster (1.00-1.02 against 0.92 of copy bandwidth on a 64 x 32-head bf16 batch; at
   // head_dim 64 0.91 with paired KV heads against 0.86).
-  // f32 caches take the tf32 kernel from 5 query heads per KV head (at 8: 0.82 of copy
-  // bandwidth against 0.36 on CUDA cores, head_dim 128); up to 4 the CUDA-core kernel
-  // streams faster (0.92 against 0.84 at 4) with no conversion work.
+  // f32 caches take the tf32 kernel at head_dim 128 from 5 query heads per KV head (at
+  // 5 to 8: 0.82 of copy bandwidth against 0.36-0.37 on CUDA cores); up to 4 the CUDA-core
+  // kernel streams faster (0.92 against 0.84 at 4) with no conversion work, and at head_dim
+  // 64 it is as fast or a little faster at every group (0.53-0.54 against 0.53 at 5 to 8).
   if (path == PKV_PATH_AUTO)
-    path = tc_ok && (c->dtype != PKV_F32 || group >= 5) ? PKV_PATH_TENSOR_CORE : PKV_PATH_CUDA_CORE;
+    path = tc_ok && (c->dtype != PKV_F32 || (group >= 5 && c->head_dim == 128)) ? PKV_PATH_TENSOR_CORE
+                                                                                : PKV_PATH_CUDA_CORE;
   if (path == PKV_PATH_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED,
                 "tensor-core path needs head_dim 64 or 128 and group <= 16 (<= 8 for f32) (group %d)", group);

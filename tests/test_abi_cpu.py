@@ -156,13 +156,17 @@ def test_plan_reports_path_partitions_and_launches(lib):
     assert pkv.paged_attention_plan(128, 8, 2048, k16b64)["path"] == pkv.PATH_TENSOR_CORE  # 64-token blocks
     k32b64 = torch.empty((1, 8, 64, 128), dtype=torch.float32)
     assert pkv.paged_attention_plan(32, 8, 2048, k32b64)["path"] == pkv.PATH_CUDA_CORE
-    # f32: CUDA cores up to 4 query heads per KV head, the tf32 tensor-core kernel from 5
-    # to 8 (either path on request up to 8), nothing above 8
+    # f32: at head_dim 128 CUDA cores up to 4 query heads per KV head, the tf32
+    # tensor-core kernel from 5 to 8; at head_dim 64 CUDA cores up to 8 (either path on
+    # request up to 8), nothing above 8
+    k32d128 = torch.empty((1, 8, 16, 128), dtype=torch.float32)
     assert pkv.paged_attention_plan(64, 8, 2048, k32, path=pkv.PATH_TENSOR_CORE)["path"] == pkv.PATH_TENSOR_CORE
-    assert pkv.paged_attention_plan(64, 32, 2048, k32)["path"] == pkv.PATH_CUDA_CORE     # group 4
-    assert pkv.paged_attention_plan(64, 40, 2048, k32)["path"] == pkv.PATH_TENSOR_CORE   # group 5
-    assert pkv.paged_attention_plan(64, 64, 2048, k32)["path"] == pkv.PATH_TENSOR_CORE   # group 8
-    assert pkv.paged_attention_plan(64, 24, 2048, k32)["path"] == pkv.PATH_CUDA_CORE     # group 3
+    assert pkv.paged_attention_plan(64, 32, 2048, k32d128)["path"] == pkv.PATH_CUDA_CORE  # group 4
+    assert pkv.paged_attention_plan(64, 40, 2048, k32d128)["path"] == pkv.PATH_TENSOR_CORE  # group 5
+    assert pkv.paged_attention_plan(64, 64, 2048, k32d128)["path"] == pkv.PATH_TENSOR_CORE  # group 8
+    assert pkv.paged_attention_plan(64, 24, 2048, k32d128)["path"] == pkv.PATH_CUDA_CORE  # group 3
+    assert pkv.paged_attention_plan(64, 40, 2048, k32)["path"] == pkv.PATH_CUDA_CORE     # head_dim 64, group 5
+    assert pkv.paged_attention_plan(64, 64, 2048, k32)["path"] == pkv.PATH_CUDA_CORE     # head_dim 64, group 8
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_attention_plan(64, 72, 2048, k32, path=pkv.PATH_TENSOR_CORE)          # group 9
     with pytest.raises(pkv.PagedKVError):   # f32 at group 16: above the CUDA-core path's 8
